@@ -1,0 +1,212 @@
+/*
+ * muon.h -- C ABI of libmuon.so, the GB300 (sm_103a) Muon optimizer step.
+ *
+ * One Muon step of a set of 2-D logical matrices: fp32 momentum update with
+ * optional Nesterov look-ahead, Frobenius normalisation, five (ns_steps)
+ * Newton-Schulz quintic iterations on the full matrix, and the weight update
+ *     W <- W - lr * (sqrt(max(1, rows/cols)) * U + wd * W).
+ * Sources: "Muon Optimizer + FSDP" (section 背景: M_t = momentum_update(grad),
+ * U_t = NewtonSchulz(M_t), W_t = W_t - lr U_t; section 分块通信: micro-buckets of
+ * whole matrices, fused [Q;K;V] and [E,out,in] tensors split into logical
+ * matrices; section 内存控制方案 items 1-4: bucket cap, one persistent
+ * preallocated workspace, bounded in-flight buckets, bf16 buffers with fp32
+ * normalisation scalars); DeepSpeed issue "[RFC] Enable Correct and
+ * High-Performance Muon Optimizer under ZeRO CPU Offload" (section 2: 5-6
+ * Newton-Schulz iterations on full 2-D matrices; section 4.A: shapes and head
+ * dimensions carried with the tensors; section 4.D: per-head Muon on
+ * interleaved QKV); DeepSpeed PR "[Muon] CPU offload: pin the momentum and
+ * overlap the host writeback" (section Changes: pinned momentum, writeback of
+ * batch i on a side stream overlapping batch i+1, drained before the host
+ * reads).
+ *
+ * Conventions for every entry point:
+ *  - No C++ exception and no CUDA error escapes: each call returns a
+ *    muon_status.  0 is success, < 0 an error (nothing was enqueued unless the
+ *    text says so), > 0 a warning.
+ *  - The caller owns every tensor and the workspace memory; the plan owns only
+ *    host metadata, CUDA events and its private streams.  No entry point
+ *    allocates device memory.
+ *  - "stream" arguments are cudaStream_t values passed as void* (NULL = the
+ *    legacy default stream).  Device work is enqueued asynchronously and in
+ *    stream order; device-side faults of that work (a bounded wait that ran
+ *    out, a non-finite matrix) are reported by muon_sync.
+ *  - Matrices are row-major, contiguous within a matrix.  Device pointers
+ *    must be 16-byte aligned.
+ */
+#ifndef MUON_H
+#define MUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t muon_status;
+
+#define MUON_OK 0
+#define MUON_WARN_NONFINITE 1   /* some matrix had a non-finite norm; see muon_sync */
+#define MUON_ERR_INVALID (-1)   /* bad argument: null, size, dtype, alignment, count */
+#define MUON_ERR_NOT_PINNED (-2) /* offload host buffer is not page-locked */
+#define MUON_ERR_NO_WORKSPACE (-3) /* no workspace bound, or it is too small */
+#define MUON_ERR_CUDA (-4)      /* a CUDA runtime/driver call failed */
+#define MUON_ERR_TIMEOUT (-5)   /* a bounded host wait ran out */
+#define MUON_ERR_UNSUPPORTED (-6) /* option not available in this build / device */
+#define MUON_ERR_DEVICE (-7)    /* a kernel's bounded wait ran out (device status word) */
+
+/* element types */
+#define MUON_DTYPE_F32 0
+#define MUON_DTYPE_BF16 1
+
+/* Newton-Schulz arithmetic */
+#define MUON_NS_BF16 0    /* bf16 operands, fp32 accumulation (tcgen05 kind::f16) */
+#define MUON_NS_TF32X3 1  /* fp32 storage, 3xTF32 split products (tcgen05 kind::tf32) */
+
+/* momentum form (the pages name momentum_update without a formula) */
+#define MUON_MOMENTUM_EMA 0 /* M <- mu M + (1-mu) G;  Nesterov V = (1-mu) G + mu M */
+#define MUON_MOMENTUM_SGD 1 /* M <- mu M + G;         Nesterov V = G + mu M        */
+
+typedef struct muon_plan_s muon_plan_t;
+
+/* One tensor holding `count` logical rows x cols matrices, `stride_elems`
+ * elements apart (0 means rows*cols: contiguous [count, rows, cols]).
+ * An expert tensor [E, out, in] is {out, in, E, 0}; a fused projection of H
+ * heads of D rows is {D, in, H, 0}; a plain matrix is {rows, cols, 1, 0}. */
+typedef struct {
+  int64_t rows;
+  int64_t cols;
+  int64_t count;
+  int64_t stride_elems;
+} muon_shape;
+
+typedef struct {
+  float ns_a, ns_b, ns_c;   /* quintic coefficients: X' = a X + (b A + c A A) X */
+  float eps;                /* X0 = V / (||V||_F + eps) */
+  int32_t ns_precision;     /* MUON_NS_BF16 or MUON_NS_TF32X3 */
+  int32_t momentum_form;    /* MUON_MOMENTUM_EMA or MUON_MOMENTUM_SGD */
+  int32_t grad_dtype;       /* MUON_DTYPE_BF16 or MUON_DTYPE_F32 */
+  int32_t param_dtype;      /* MUON_DTYPE_F32 or MUON_DTYPE_BF16 (weights) */
+  int32_t max_inflight;     /* offload: buckets whose writeback may be in flight (1 or 2) */
+  int32_t skip_nonfinite;   /* 1: a matrix whose Newton-Schulz input has a non-finite norm
+                               leaves its weights untouched (its momentum keeps the
+                               non-finite values; muon_sync reports the count) */
+  int32_t timing;           /* 1: record per-bucket CUDA events for muon_get_stats */
+  int32_t offload;          /* 1: reserve host-link staging slots for muon_offload_step */
+  int32_t reserved[4];
+} muon_config;
+
+/* Fills *cfg with (3.4445, -4.7750, 2.0315), eps 1e-7, bf16 NS, EMA momentum,
+ * bf16 gradients, fp32 weights, max_inflight 1, skip_nonfinite 1, timing 0,
+ * offload 0. */
+void muon_config_default(muon_config* cfg);
+
+/* Builds the host plan: orients each logical matrix (wide form m x n, m <= n,
+ * transposed when rows > cols), groups matrices by (group label, m, n), and
+ * packs whole matrices, in order, into micro-buckets whose wide-form bf16 bytes
+ * (m*n*2 summed) stay <= bucket_cap_bytes.  A matrix larger than the cap gets a
+ * bucket of its own.  bucket_cap_bytes <= 0 puts everything in one bucket.
+ *   shapes[n_shapes]: tensor descriptions (copied).
+ *   groups: NULL (group by wide shape only) or n_shapes labels; matrices with
+ *           different labels never share a bucket.
+ *   cfg:    NULL for muon_config_default.
+ *   out:    receives the plan; free it with muon_plan_destroy.
+ * Pure host work: needs no GPU.  Errors: MUON_ERR_INVALID. */
+muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t* groups,
+                      int64_t bucket_cap_bytes, const muon_config* cfg, muon_plan_t** out);
+
+/* Device workspace the plan needs (bytes, 256-byte aligned use), including the
+ * offload staging slots.  Pure host work. */
+muon_status muon_plan_workspace_bytes(const muon_plan_t* plan, size_t* device_bytes);
+
+/* Binds caller-allocated device memory of at least muon_plan_workspace_bytes,
+ * 256-byte aligned, on the current device.  Encodes the TMA tensor maps over
+ * it and creates the plan's events/streams.  The memory must outlive every
+ * enqueued step.  Errors: MUON_ERR_INVALID, MUON_ERR_NO_WORKSPACE, MUON_ERR_CUDA,
+ * MUON_ERR_UNSUPPORTED (device is not sm_103). */
+muon_status muon_plan_bind_workspace(muon_plan_t* plan, void* dev_ptr, size_t bytes);
+
+/* One Muon step over every matrix of the plan, enqueued on `stream`.
+ *   params[n_mats]:   device pointers, weights (cfg.param_dtype), updated in place.
+ *   grads[n_mats]:    device pointers, gradients (cfg.grad_dtype), read only.
+ *   momentum[n_mats]: device pointers, fp32 momentum, updated in place.
+ *   n_mats:           number of pointers in each array = n_shapes of the plan;
+ *                     entry i covers all `count` logical matrices of shapes[i].
+ *   lr, mu, wd:       learning rate, momentum, decoupled weight decay.
+ *   nesterov:         0 / 1.
+ *   ns_steps:         Newton-Schulz iterations (0..16); the pages use 5-6.
+ * Arguments are validated before anything is enqueued.  The buffers of one
+ * entry must not overlap another entry's.  Returns MUON_OK after enqueueing. */
+muon_status muon_step(muon_plan_t* plan, void* const* params, const void* const* grads,
+                      void* const* momentum, int64_t n_mats, float lr, float mu,
+                      int32_t nesterov, float wd, int32_t ns_steps, void* stream);
+
+/* Offload step: gradients and fp32 momentum live in page-locked host memory.
+ * Per micro-bucket: host->device copy of G and M on a private copy stream,
+ * momentum + Newton-Schulz on `compute`, then device->host writeback of the new
+ * momentum (into h_momentum) and of the update U' = sqrt(max(1,rows/cols)) * U
+ * (fp32, original orientation, into h_update_out) on the side stream `copy`,
+ * overlapping the next bucket's Newton-Schulz.  At most cfg.max_inflight
+ * buckets are in writeback while one computes.  The host then applies
+ * W -= lr * (U' + wd * W) itself.  Blocks until every writeback has landed
+ * (the host reads the results next) or timeout_ms passes (MUON_ERR_TIMEOUT).
+ *   h_grads / h_momentum / h_update_out [n_mats]: pinned host pointers laid out
+ *   like the device tensors of muon_step.  MUON_ERR_NOT_PINNED if any is not
+ *   page-locked. */
+muon_status muon_offload_step(muon_plan_t* plan, const void* const* h_grads,
+                              void* const* h_momentum, void* const* h_update_out,
+                              int64_t n_mats, float mu, int32_t nesterov, int32_t ns_steps,
+                              void* compute, void* copy, int64_t timeout_ms);
+
+/* Waits for `stream`, then reads and clears the device status word written by
+ * the kernels: MUON_ERR_DEVICE if a kernel's bounded wait ran out,
+ * MUON_WARN_NONFINITE (with *n_nonfinite set) if a matrix norm was not finite,
+ * else MUON_OK.  n_nonfinite may be NULL. */
+muon_status muon_sync(muon_plan_t* plan, void* stream, int64_t* n_nonfinite);
+
+/* Plan layout, for logging and tests (pure host). */
+typedef struct {
+  int64_t n_tensors;
+  int64_t n_matrices;
+  int64_t n_groups;        /* distinct (label, m, n) */
+  int64_t n_buckets;
+  int64_t max_bucket_matrices;
+  int64_t max_bucket_bytes; /* wide-form bf16 bytes of the largest bucket */
+  size_t workspace_bytes;
+} muon_plan_info;
+muon_status muon_get_plan_info(const muon_plan_t* plan, muon_plan_info* info);
+
+/* Bucket b: number of matrices, wide-form bf16 bytes, same-shape groups in it,
+ * and the (m, n) of its first group. */
+typedef struct {
+  int64_t n_matrices;
+  int64_t bytes;
+  int64_t n_groups;
+  int64_t m, n;
+} muon_bucket_info;
+muon_status muon_get_bucket_info(const muon_plan_t* plan, int64_t b, muon_bucket_info* info);
+
+/* Timings of the last step (cfg.timing = 1), summed over buckets, in ms:
+ * prep (momentum kernel), ns (all Newton-Schulz GEMMs), apply, h2d, d2h and the
+ * whole step; plus bytes moved over the host link.  Synchronizes the events. */
+typedef struct {
+  double prep_ms, ns_ms, apply_ms, h2d_ms, d2h_ms, step_ms;
+  int64_t h2d_bytes, d2h_bytes;
+  int64_t n_buckets;
+} muon_stats;
+muon_status muon_get_stats(const muon_plan_t* plan, muon_stats* out);
+
+/* Text of the last error reported by an entry point on the calling thread
+ * (empty string if none).  Valid until that thread's next call. */
+const char* muon_last_error(void);
+
+/* Static description of a status code. */
+const char* muon_status_string(muon_status s);
+
+/* Frees the plan's host memory, events and streams (not the workspace). */
+void muon_plan_destroy(muon_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MUON_H */

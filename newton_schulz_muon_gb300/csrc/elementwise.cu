@@ -1,0 +1,379 @@
+// HBM-bound kernels of the Muon step on sm_103a:
+//
+//  * momentum_prep: fused fp32 momentum update (EMA or SGD form) with optional
+//    Nesterov look-ahead, sum of squares of the Newton-Schulz input V for the
+//    Frobenius norm (warp shuffles, fixed-order block reduction, one partial per
+//    tile), and the bf16 (or tf32 hi/lo) cast of V into the workspace in wide
+//    orientation (transposed through shared memory when rows > cols).
+//    Sources: "Muon Optimizer + FSDP", section 背景 (M_t = momentum_update(grad)
+//    feeds NewtonSchulz); section 内存控制方案 item 4 (bf16 Newton-Schulz buffers,
+//    normalisation scalars kept in fp32).
+//  * norm_finalize: per matrix, sums its tile partials in a fixed order (fp64),
+//    and stores s = 1 / (||V||_F + eps) and a non-finite flag.  s is folded into
+//    the first Newton-Schulz iteration's GEMM epilogues instead of rescaling X0.
+//  * apply: W <- W - lr (sqrt(max(1, rows/cols)) U + wd W), un-transposing U
+//    through shared memory for tall matrices ("Muon Optimizer + FSDP", 背景:
+//    W_t = W_t - lr * U_t); or, for the offload path, U' = sqrt(max(1,rows/cols)) U
+//    written in fp32 for the host.
+//
+// Every kernel works on 64 x 64 tiles of one logical matrix (rows x cols, the
+// caller's layout).  Full tiles of aligned matrices use 16-byte accesses.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "device.cuh"
+#include "kernels.h"
+
+namespace muon {
+namespace {
+
+constexpr int kT = kPrepTile;       // 64
+constexpr int kThreads = 256;       // 16 x 16 threads, 4 x 4 elements each
+
+// ---------------------------------------------------------------------------
+// fp32 momentum with the rounding of one correctly rounded operation:
+// mu*m and w*g are split exactly into (high, low) pairs with fma, then added
+// as double-word numbers (Joldes, Muller, Popescu, "Tight and rigorous error
+// bounds for basic building blocks of double-word arithmetic", 2017, accurate
+// DW+DW).  The high word of the result is within 3u^2 relative of the exact
+// value, so it is the nearest float or its neighbour: within 1 ulp.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  const float ap = __fsub_rn(s, bp);
+  e = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
+}
+
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  e = __fsub_rn(b, __fsub_rn(s, a));
+}
+
+__device__ __forceinline__ float dot2_accurate(float mu, float m, float w, float g) {
+  const float ph = __fmul_rn(mu, m), pl = __fmaf_rn(mu, m, -ph);
+  const float qh = __fmul_rn(w, g), ql = __fmaf_rn(w, g, -qh);
+  float sh, sl, th, tl, vh, vl, zh, zl;
+  two_sum(ph, qh, sh, sl);
+  two_sum(pl, ql, th, tl);
+  fast_two_sum(sh, __fadd_rn(sl, th), vh, vl);
+  fast_two_sum(vh, __fadd_rn(tl, vl), zh, zl);
+  return zh;
+}
+
+struct Tile {
+  int seg;
+  int64_t mat;   // matrix within the run
+  int64_t r0, c0;
+};
+
+template <typename Seg>
+__device__ __forceinline__ Tile decode_tile(const Seg* segs, int n_segs, int64_t t) {
+  int lo = 0, hi = n_segs - 1;
+  while (lo < hi) {  // last segment with block0 <= t
+    const int mid = (lo + hi + 1) >> 1;
+    if (segs[mid].block0 <= t) lo = mid; else hi = mid - 1;
+  }
+  const Seg& s = segs[lo];
+  const int64_t local = t - s.block0;
+  Tile tile;
+  tile.seg = lo;
+  tile.mat = local / s.tiles_per_mat;
+  const int64_t tt = local % s.tiles_per_mat;
+  tile.r0 = (tt / s.tiles_c) * kT;
+  tile.c0 = (tt % s.tiles_c) * kT;
+  return tile;
+}
+
+__device__ __forceinline__ float load_grad(const void* g, int64_t i, int dtype) {
+  if (dtype == 1) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(g)[i]);
+  return reinterpret_cast<const float*>(g)[i];
+}
+
+__device__ __forceinline__ void store_x(void* x_hi, float* x_lo, int64_t i, float v, int tf32) {
+  if (tf32) {
+    const float h = round_tf32(v);
+    reinterpret_cast<float*>(x_hi)[i] = h;
+    x_lo[i] = v - h;
+  } else {
+    reinterpret_cast<__nv_bfloat16*>(x_hi)[i] = __float2bfloat16_rn(v);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_constant__ PrepArgs a) {
+  __shared__ float vt[kT][kT + 1];
+  __shared__ float red[kThreads / 32];
+  const int64_t t = blockIdx.x;
+  if (t >= a.total_tiles) return;
+  const Tile tile = decode_tile(a.seg, a.n_segs, t);
+  const PrepSeg& s = a.seg[tile.seg];
+  const int64_t rows = s.rows, cols = s.cols;
+  const int64_t base = tile.mat * s.stride;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const float mu = a.mu, omu = a.omu;
+  float sumsq = 0.f;
+  float v[4][4];
+
+  const bool full = (tile.r0 + kT <= rows) && (tile.c0 + kT <= cols);
+  const bool vec = full && ((cols & 3) == 0) && ((s.stride & 3) == 0);
+  float* mrow = s.m + base;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t r = tile.r0 + ty + 16 * k;
+    const int64_t c = tile.c0 + 4 * tx;
+    if (vec) {
+      const int64_t off = r * cols + c;
+      float4 mv = *reinterpret_cast<const float4*>(mrow + off);
+      float gv[4];
+      if (a.grad_dtype == 1) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(
+            reinterpret_cast<const __nv_bfloat16*>(s.g) + base + off);
+        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        gv[0] = __low2float(g01); gv[1] = __high2float(g01);
+        gv[2] = __low2float(g23); gv[3] = __high2float(g23);
+      } else {
+        const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(s.g) + base + off);
+        gv[0] = f.x; gv[1] = f.y; gv[2] = f.z; gv[3] = f.w;
+      }
+      float mo[4] = {mv.x, mv.y, mv.z, mv.w};
+      float mn[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        mn[j] = dot2_accurate(mu, mo[j], omu, gv[j]);
+        v[k][j] = a.nesterov ? __fmaf_rn(mu, mn[j], __fmul_rn(omu, gv[j])) : mn[j];
+        sumsq = __fmaf_rn(v[k][j], v[k][j], sumsq);
+      }
+      *reinterpret_cast<float4*>(mrow + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[k][j] = 0.f;
+        if (r < rows && c + j < cols) {
+          const int64_t off = r * cols + c + j;
+          const float gj = load_grad(s.g, base + off, a.grad_dtype);
+          const float mn = dot2_accurate(mu, mrow[off], omu, gj);
+          mrow[off] = mn;
+          v[k][j] = a.nesterov ? __fmaf_rn(mu, mn, __fmul_rn(omu, gj)) : mn;
+          sumsq = __fmaf_rn(v[k][j], v[k][j], sumsq);
+        }
+      }
+    }
+  }
+
+  // X0 = cast(V) in wide orientation (the 1/(||V||+eps) factor is applied later).
+  const int64_t xb = tile.mat * s.x_mstride;
+  if (!s.transposed) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t r = tile.r0 + ty + 16 * k;
+      const int64_t c = tile.c0 + 4 * tx;
+      if (full && !a.tf32) {
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(v[k][0], v[k][1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(v[k][2], v[k][3]);
+        uint2 raw;
+        raw.x = *reinterpret_cast<uint32_t*>(&p0);
+        raw.y = *reinterpret_cast<uint32_t*>(&p1);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(s.x_hi) + xb + r * s.x_ld + c) = raw;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (r < rows && c + j < cols) store_x(s.x_hi, s.x_lo, xb + r * s.x_ld + c + j, v[k][j], a.tf32);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vt[ty + 16 * k][4 * tx + j] = v[k][j];
+    __syncthreads();
+    // X[c][r] = V[r][c]: X row = source column, X column = source row.
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int xi = ty + 16 * k;        // source column within the tile
+      const int64_t xr = tile.c0 + xi;   // X row
+      const int64_t xc = tile.r0 + 4 * tx;
+      float w4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w4[j] = vt[4 * tx + j][xi];
+      if (full && !a.tf32) {
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(w4[0], w4[1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(w4[2], w4[3]);
+        uint2 raw;
+        raw.x = *reinterpret_cast<uint32_t*>(&p0);
+        raw.y = *reinterpret_cast<uint32_t*>(&p1);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(s.x_hi) + xb + xr * s.x_ld + xc) = raw;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (xr < cols && xc + j < rows) store_x(s.x_hi, s.x_lo, xb + xr * s.x_ld + xc + j, w4[j], a.tf32);
+      }
+    }
+  }
+
+  sumsq = warp_sum(sumsq);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sumsq;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
+    a.partials[t] = tot;
+  }
+}
+
+// One warp per matrix: fixed-order fp64 sum of its tile partials.
+__global__ void norm_finalize_kernel(const __grid_constant__ PrepArgs a) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= a.n_mats) return;
+  int si = 0;
+  for (int i = 1; i < a.n_segs; ++i)
+    if (a.seg[i].mat0 <= warp) si = i;
+  const PrepSeg& s = a.seg[si];
+  const int64_t first = s.block0 + (int64_t)(warp - s.mat0) * s.tiles_per_mat;
+  double acc = 0.0;
+  for (int64_t i = lane; i < s.tiles_per_mat; i += 32) acc += (double)a.partials[first + i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    const bool finite = isfinite(acc);
+    a.scale[warp] = finite ? (float)(1.0 / (sqrt(acc) + (double)a.eps)) : 0.f;
+    a.flags[warp] = finite ? 0 : 1;
+    if (!finite) atomicAdd(&a.status->nonfinite, 1u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// apply / emit
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float load_u(const void* hi, const float* lo, int64_t i, int tf32) {
+  if (tf32) return reinterpret_cast<const float*>(hi)[i] + lo[i];
+  return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(hi)[i]);
+}
+
+__global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__ ApplyArgs a) {
+  __shared__ float ut[kT][kT + 1];
+  const int64_t t = blockIdx.x;
+  if (t >= a.total_tiles) return;
+  const Tile tile = decode_tile(a.seg, a.n_segs, t);
+  const ApplySeg& s = a.seg[tile.seg];
+  const int mat = s.mat0 + (int)tile.mat;
+  if (!a.emit && a.skip_nonfinite && a.flags[mat]) return;  // whole tile belongs to one matrix
+  const int64_t rows = s.rows, cols = s.cols;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int64_t ub = tile.mat * s.u_mstride;
+  const float us = a.unnormalized ? a.scale[mat] : 1.0f;
+  const bool full = (tile.r0 + kT <= rows) && (tile.c0 + kT <= cols);
+  float u[4][4];
+
+  if (s.transposed) {
+    // U_wide is cols x rows; gather the tile's transpose through shared memory.
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int wi = ty + 16 * k;            // wide row = W column
+      const int64_t wr = tile.c0 + wi;
+      const int64_t wc = tile.r0 + 4 * tx;   // wide column = W row
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ut[wi][4 * tx + j] = (wr < cols && wc + j < rows) ? load_u(s.u_hi, s.u_lo, ub + wr * s.u_ld + wc + j, a.tf32) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) u[k][j] = ut[4 * tx + j][ty + 16 * k];
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t r = tile.r0 + ty + 16 * k;
+      const int64_t c = tile.c0 + 4 * tx;
+      if (full && !a.tf32) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(
+            reinterpret_cast<const __nv_bfloat16*>(s.u_hi) + ub + r * s.u_ld + c);
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        u[k][0] = __low2float(p0); u[k][1] = __high2float(p0);
+        u[k][2] = __low2float(p1); u[k][3] = __high2float(p1);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          u[k][j] = (r < rows && c + j < cols) ? load_u(s.u_hi, s.u_lo, ub + r * s.u_ld + c + j, a.tf32) : 0.f;
+      }
+    }
+  }
+
+  const int64_t wb = tile.mat * s.stride;
+  const float sc = s.shape_scale;
+  const bool vec = full && ((cols & 3) == 0) && ((s.stride & 3) == 0);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t r = tile.r0 + ty + 16 * k;
+    const int64_t c = tile.c0 + 4 * tx;
+    const int64_t off = wb + r * cols + c;
+    if (a.emit) {
+      float* out = reinterpret_cast<float*>(s.w);
+      if (vec) {
+        *reinterpret_cast<float4*>(out + off) =
+            make_float4(sc * (us * u[k][0]), sc * (us * u[k][1]), sc * (us * u[k][2]), sc * (us * u[k][3]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (r < rows && c + j < cols) out[off + j] = sc * (us * u[k][j]);
+      }
+      continue;
+    }
+    if (a.param_dtype == 0) {
+      float* w = reinterpret_cast<float*>(s.w);
+      if (vec) {
+        float4 w4 = *reinterpret_cast<const float4*>(w + off);
+        float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          wv[j] = __fmaf_rn(-a.lr, __fmaf_rn(sc, us * u[k][j], __fmul_rn(a.wd, wv[j])), wv[j]);
+        *reinterpret_cast<float4*>(w + off) = make_float4(wv[0], wv[1], wv[2], wv[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (r < rows && c + j < cols) {
+            const float wv = w[off + j];
+            w[off + j] = __fmaf_rn(-a.lr, __fmaf_rn(sc, us * u[k][j], __fmul_rn(a.wd, wv)), wv);
+          }
+      }
+    } else {
+      __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(s.w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (r < rows && c + j < cols) {
+          const float wv = __bfloat162float(w[off + j]);
+          w[off + j] = __float2bfloat16_rn(
+              __fmaf_rn(-a.lr, __fmaf_rn(sc, us * u[k][j], __fmul_rn(a.wd, wv)), wv));
+        }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
+  if (a.total_tiles <= 0) return cudaSuccess;
+  momentum_prep_kernel<<<(unsigned)a.total_tiles, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm(const PrepArgs& a, cudaStream_t s) {
+  if (a.n_mats <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = (a.n_mats * 32 + threads - 1) / threads;
+  norm_finalize_kernel<<<blocks, threads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t s) {
+  if (a.total_tiles <= 0) return cudaSuccess;
+  apply_kernel<<<(unsigned)a.total_tiles, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace muon

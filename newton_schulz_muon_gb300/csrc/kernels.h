@@ -1,0 +1,133 @@
+// Kernel argument blocks and launchers shared by the host runtime and the
+// kernels of libmuon.so.  Arguments travel by value as kernel parameters
+// (tensor maps as __grid_constant__), so nothing here is read from the host.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace muon {
+
+constexpr int kMaxSegs = 64;     // runs of consecutive matrices of one tensor per bucket
+constexpr int kMaxGroups = 4;    // same-shape groups per bucket (one grouped GEMM launch)
+constexpr int kPrepTile = 64;    // momentum / apply tiles are 64 x 64 elements
+
+// Workspace header (offset 0): device status word and non-finite counter.
+struct DeviceStatus {
+  unsigned flags;       // kStatusWaitTimeout, ...
+  unsigned nonfinite;   // matrices with a non-finite norm since the last muon_sync
+};
+
+// ---------------------------------------------------------------------------
+// momentum + prep (one run of `count` matrices of one tensor)
+// ---------------------------------------------------------------------------
+struct PrepSeg {
+  const void* g;         // gradient of the run's first matrix
+  float* m;              // fp32 momentum of the run's first matrix (updated in place)
+  void* x_hi;            // workspace X0 of the run's first matrix (bf16, or tf32-hi fp32)
+  float* x_lo;           // tf32-lo part (3xTF32 mode), else null
+  int64_t rows, cols;    // logical shape
+  int64_t stride;        // elements between consecutive matrices in g and m
+  int64_t x_ld;          // leading dimension of X (wide form m x n)
+  int64_t x_mstride;     // elements between consecutive matrices in X
+  int64_t block0;        // first tile index of the run in the bucket's tile space
+  int32_t count;         // matrices in the run
+  int32_t transposed;    // 1 when rows > cols: X = V^T
+  int32_t tiles_c;       // 64-wide tiles along cols
+  int32_t tiles_per_mat; // tiles per matrix
+  int32_t mat0;          // bucket-local index of the run's first matrix
+  int32_t pad_;
+};
+
+struct PrepArgs {
+  PrepSeg seg[kMaxSegs];
+  int32_t n_segs;
+  int32_t n_mats;        // matrices in the bucket
+  int64_t total_tiles;
+  float mu, omu;         // momentum and its complement (1 for the SGD form)
+  int32_t nesterov;
+  int32_t grad_dtype;    // 0 fp32, 1 bf16
+  int32_t tf32;          // 1: write X0 as tf32 hi/lo fp32 pair
+  float eps;
+  float* partials;       // one fp32 sum of squares per tile
+  float* scale;          // per matrix: 1 / (||V||_F + eps)
+  int32_t* flags;        // per matrix: 1 if the norm was not finite
+  DeviceStatus* status;
+};
+
+// ---------------------------------------------------------------------------
+// apply / emit (one run of matrices)
+// ---------------------------------------------------------------------------
+struct ApplySeg {
+  void* w;               // weights (apply) or fp32 U' output (emit) of the first matrix
+  const void* u_hi;      // final X of the first matrix (bf16 or tf32-hi fp32)
+  const float* u_lo;     // tf32-lo part, or null
+  int64_t rows, cols, stride;
+  int64_t u_ld, u_mstride;
+  int64_t block0;
+  int32_t count, transposed, tiles_c, tiles_per_mat, mat0;
+  float shape_scale;     // sqrt(max(1, rows/cols))
+};
+
+struct ApplyArgs {
+  ApplySeg seg[kMaxSegs];
+  int32_t n_segs;
+  int64_t total_tiles;
+  float lr, wd;
+  int32_t param_dtype;   // 0 fp32, 1 bf16
+  int32_t tf32;
+  int32_t emit;          // 1: write U' = shape_scale * U (fp32) instead of updating W
+  int32_t skip_nonfinite;
+  int32_t unnormalized;  // 1 when no NS iteration ran: U = scale * X0
+  const float* scale;
+  const int32_t* flags;
+};
+
+// ---------------------------------------------------------------------------
+// Newton-Schulz GEMMs (tcgen05)
+// ---------------------------------------------------------------------------
+enum GemmMode : int32_t { kGram = 0, kPoly = 1, kUpdate = 2 };
+
+struct GemmGroup {
+  CUtensorMap map_a;     // operand A (K-major, box {64 (k), 128 rows})
+  CUtensorMap map_b;     // operand B (K-major box {64, 128} x2, or MN-major box {64, 64} x4)
+  CUtensorMap map_a_lo;  // 3xTF32: low parts (unused in bf16 mode)
+  CUtensorMap map_b_lo;
+  void* c_hi;            // output (bf16 or tf32-hi fp32)
+  float* c_lo;           // output tf32-lo part
+  const void* d_hi;      // epilogue addend (POLY: A, UPDATE: X)
+  const float* d_lo;
+  int64_t c_ld, c_mstride;   // elements
+  int32_t M, N, K;           // output rows, cols, reduction length
+  int32_t count;             // matrices
+  int32_t tiles_m, tiles_n;  // tile grid of one matrix
+  int32_t tiles_per_mat;     // tiles computed per matrix (upper triangle for GRAM/POLY)
+  int32_t tile0;             // first launch-wide tile index of this group
+  int32_t mat_base;          // bucket-local index of matrix 0 (for the scale array)
+  int32_t pad_[3];
+};
+
+struct GemmArgs {
+  GemmGroup g[kMaxGroups];
+  int32_t n_groups;
+  int32_t total_tiles;
+  int32_t mode;
+  int32_t use_scale;      // first iteration: fold 1/(||V||+eps) into the epilogue
+  float alpha, beta;      // GRAM: 1, -; POLY: c, b; UPDATE: 1, a
+  const float* scale;     // per bucket-local matrix
+  DeviceStatus* status;
+};
+
+// GEMM tile shape (bf16): 128 x 256 outputs per CTA, 64-deep k blocks.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+
+// launchers (return the launch's cudaError_t)
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_norm(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t s);
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, cudaStream_t s);
+size_t gemm_smem_bytes(bool tf32);
+
+}  // namespace muon

@@ -1,0 +1,907 @@
+// Host runtime of libmuon.so: the C ABI declared in include/muon.h.
+//
+//  * planner   -- logical matrices of fused tensors ("Muon Optimizer + FSDP",
+//                 section 分块通信: qkv = [Q;K;V] and experts [E,out,in] are split
+//                 into logical matrices; DeepSpeed issue #8463 section 4.A: shapes
+//                 and head dimensions carried into the optimizer), wide orientation,
+//                 same-shape groups across layers (section 内存控制方案 item 6), and
+//                 micro-buckets of whole matrices under a byte cap (section 分块通信
+//                 and item 1).
+//  * workspace -- one persistent region sized for the largest micro-bucket and
+//                 reused by every bucket through offsets (item 2, "preallocate and
+//                 reuse"); the caller allocates it, the plan never does.
+//  * step      -- per bucket: momentum prep, norm finalize, ns_steps x (GRAM, POLY,
+//                 UPDATE), apply; all stream-ordered, no host synchronisation.
+//  * offload   -- DeepSpeed PR "[Muon] CPU offload: pin the momentum and overlap
+//                 the host writeback", section Changes: pinned host momentum and
+//                 gradients, host->device copy per bucket, writeback of bucket i on
+//                 a side stream while bucket i+1 computes, at most max_inflight
+//                 buckets in flight, drained before the host reads.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <new>
+#include <string>
+#include <thread>
+#include <tuple>
+#include <vector>
+
+#include "kernels.h"
+#include "muon.h"
+
+using namespace muon;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+muon_status fail(muon_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+muon_status fail(muon_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+muon_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MUON_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 1024;
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct TensorInfo {
+  int64_t rows, cols, count, stride;
+  int64_t m, n;
+  bool transposed;
+  int label;
+  int group;
+};
+
+struct Run {  // matrices [first, first+count) of tensor `tensor`
+  int tensor;
+  int64_t first, count;
+};
+
+struct BGroup {
+  int group;
+  int64_t m, n, count;
+  int64_t mat_base;      // bucket-local index of the group's first matrix
+  int64_t ld_n, ld_m;    // leading dimensions in the workspace
+  std::vector<Run> runs;
+  // byte offsets inside the NS region (hi parts; lo parts for 3xTF32)
+  size_t off_x[2], off_a, off_b;
+  size_t off_x_lo[2], off_a_lo, off_b_lo;
+  // tensor maps encoded at bind time
+  CUtensorMap kx[2], mx[2], ka, kb;
+};
+
+struct Bucket {
+  std::vector<BGroup> groups;
+  int64_t n_mats = 0, bytes = 0, elems = 0;
+  int n_runs = 0;
+  int64_t prep_tiles = 0;
+  size_t ns_bytes = 0;
+};
+
+struct BucketEvents {
+  cudaEvent_t start = nullptr, prep = nullptr, ns = nullptr, apply = nullptr, h2d = nullptr,
+              d2h_start = nullptr, d2h = nullptr;
+};
+
+}  // namespace
+
+struct muon_plan_s {
+  muon_config cfg;
+  int64_t cap = 0;
+  std::vector<TensorInfo> tensors;
+  int n_groups = 0;
+  std::vector<Bucket> buckets;
+  int64_t n_matrices = 0;
+  // layout
+  size_t off_status = 0, off_scale = 0, off_flags = 0, off_partials = 0, off_ns = 0, off_stage = 0;
+  size_t ns_bytes = 0, slot_bytes = 0, ws_bytes = 0;
+  int n_slots = 0;
+  int64_t max_mats = 0, max_tiles = 0, max_elems = 0;
+  // binding
+  uint8_t* ws = nullptr;
+  size_t ws_size = 0;
+  int device = -1;
+  int num_sms = 0;
+  cudaStream_t h2d_stream = nullptr, d2h_stream = nullptr;
+  std::vector<BucketEvents> events;
+  std::vector<cudaEvent_t> slot_h2d, slot_comp, slot_d2h;
+  cudaEvent_t step_start = nullptr, step_end = nullptr;
+  bool offload_last = false;
+  int64_t last_h2d_bytes = 0, last_d2h_bytes = 0;
+};
+
+namespace {
+
+size_t elem_size_ns(const muon_config& c) { return c.ns_precision == MUON_NS_TF32X3 ? 4 : 2; }
+size_t grad_size(const muon_config& c) { return c.grad_dtype == MUON_DTYPE_BF16 ? 2 : 4; }
+size_t param_size(const muon_config& c) { return c.param_dtype == MUON_DTYPE_BF16 ? 2 : 4; }
+
+// ---------------------------------------------------------------------------
+// TMA tensor maps (driver entry point fetched through the runtime)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn) return fn;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  fn = reinterpret_cast<EncodeTiledFn>(p);
+  return fn;
+}
+
+// [count][rows][ld] array of `esize`-byte elements; logical (cols, rows, count).
+bool encode_map(CUtensorMap* map, void* base, size_t esize, int64_t cols, int64_t rows, int64_t count,
+                int64_t ld, uint32_t box_x, uint32_t box_y) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)count};
+  const cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(ld * rows * esize)};
+  const cuuint32_t box[3] = {box_x, box_y, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn(map, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// planning
+// ---------------------------------------------------------------------------
+void layout_bucket(Bucket& b, const muon_config& cfg) {
+  const size_t es = elem_size_ns(cfg);
+  const bool tf32 = cfg.ns_precision == MUON_NS_TF32X3;
+  size_t off = 0;
+  for (BGroup& g : b.groups) {
+    g.ld_n = round_up(g.n, 8);
+    g.ld_m = round_up(g.m, 8);
+    const size_t xb = (size_t)g.count * g.m * g.ld_n * es;
+    const size_t ab = (size_t)g.count * g.m * g.ld_m * es;
+    for (int i = 0; i < 2; ++i) { g.off_x[i] = off; off = align_up(off + xb, kAlign); }
+    g.off_a = off; off = align_up(off + ab, kAlign);
+    g.off_b = off; off = align_up(off + ab, kAlign);
+    if (tf32) {
+      for (int i = 0; i < 2; ++i) { g.off_x_lo[i] = off; off = align_up(off + xb, kAlign); }
+      g.off_a_lo = off; off = align_up(off + ab, kAlign);
+      g.off_b_lo = off; off = align_up(off + ab, kAlign);
+    } else {
+      g.off_x_lo[0] = g.off_x_lo[1] = g.off_a_lo = g.off_b_lo = 0;
+    }
+  }
+  b.ns_bytes = off;
+}
+
+int64_t tiles_of(int64_t rows, int64_t cols) { return cdiv(rows, kPrepTile) * cdiv(cols, kPrepTile); }
+
+muon_status build_plan(muon_plan_t* p, const muon_shape* shapes, int32_t n, const int32_t* labels) {
+  std::map<std::tuple<int, int64_t, int64_t>, int> gid;
+  for (int i = 0; i < n; ++i) {
+    const muon_shape& s = shapes[i];
+    if (s.rows <= 0 || s.cols <= 0 || s.count <= 0)
+      return fail(MUON_ERR_INVALID, "shape %d: rows, cols and count must be >= 1", i);
+    if (s.rows > (1 << 20) || s.cols > (1 << 20))
+      return fail(MUON_ERR_INVALID, "shape %d: rows/cols above 2^20 are not supported", i);
+    const int64_t stride = s.stride_elems ? s.stride_elems : s.rows * s.cols;
+    if (stride < s.rows * s.cols)
+      return fail(MUON_ERR_INVALID, "shape %d: stride_elems smaller than rows*cols", i);
+    TensorInfo t;
+    t.rows = s.rows; t.cols = s.cols; t.count = s.count; t.stride = stride;
+    t.transposed = s.rows > s.cols;
+    t.m = std::min(s.rows, s.cols);
+    t.n = std::max(s.rows, s.cols);
+    t.label = labels ? labels[i] : 0;
+    auto key = std::make_tuple(t.label, t.m, t.n);
+    auto it = gid.find(key);
+    if (it == gid.end()) it = gid.emplace(key, (int)gid.size()).first;
+    t.group = it->second;
+    p->tensors.push_back(t);
+    p->n_matrices += s.count;
+  }
+  p->n_groups = (int)gid.size();
+
+  // order: group (first appearance), tensor, matrix; pack whole matrices greedily
+  std::vector<int> order;
+  for (int g = 0; g < p->n_groups; ++g)
+    for (int i = 0; i < n; ++i)
+      if (p->tensors[i].group == g) order.push_back(i);
+
+  Bucket cur;
+  auto close = [&]() {
+    if (cur.n_mats > 0) p->buckets.push_back(cur);
+    cur = Bucket();
+  };
+  for (int ti : order) {
+    const TensorInfo& t = p->tensors[ti];
+    const int64_t mb = t.m * t.n * 2;  // wide-form bf16 bytes
+    for (int64_t j = 0; j < t.count; ++j) {
+      bool fits = cur.n_mats == 0;
+      if (!fits) {
+        const BGroup& last = cur.groups.back();
+        const bool same_group = last.group == t.group;
+        const bool same_label = p->tensors[last.runs.back().tensor].label == t.label;
+        const bool new_run = !(same_group && last.runs.back().tensor == ti &&
+                               last.runs.back().first + last.runs.back().count == j);
+        fits = same_label && (p->cap <= 0 || cur.bytes + mb <= p->cap) &&
+               (same_group || (int)cur.groups.size() < kMaxGroups) &&
+               (!new_run || cur.n_runs < kMaxSegs);
+      }
+      if (!fits) close();
+      if (cur.groups.empty() || cur.groups.back().group != t.group) {
+        BGroup g;
+        g.group = t.group; g.m = t.m; g.n = t.n; g.count = 0; g.mat_base = cur.n_mats;
+        cur.groups.push_back(g);
+      }
+      BGroup& g = cur.groups.back();
+      if (g.runs.empty() || g.runs.back().tensor != ti || g.runs.back().first + g.runs.back().count != j) {
+        g.runs.push_back(Run{ti, j, 0});
+        cur.n_runs++;
+      }
+      g.runs.back().count++;
+      g.count++;
+      cur.n_mats++;
+      cur.bytes += mb;
+      cur.elems += t.rows * t.cols;
+      cur.prep_tiles += tiles_of(t.rows, t.cols);
+    }
+  }
+  close();
+
+  // layout of the workspace
+  size_t ns_max = 0;
+  for (Bucket& b : p->buckets) {
+    layout_bucket(b, p->cfg);
+    ns_max = std::max(ns_max, b.ns_bytes);
+    p->max_mats = std::max(p->max_mats, b.n_mats);
+    p->max_tiles = std::max(p->max_tiles, b.prep_tiles);
+    p->max_elems = std::max(p->max_elems, b.elems);
+  }
+  size_t off = 0;
+  p->off_status = off; off = align_up(off + sizeof(DeviceStatus), kAlign);
+  p->off_scale = off; off = align_up(off + (size_t)p->max_mats * 4, kAlign);
+  p->off_flags = off; off = align_up(off + (size_t)p->max_mats * 4, kAlign);
+  p->off_partials = off; off = align_up(off + (size_t)p->max_tiles * 4, kAlign);
+  p->off_ns = off; off = align_up(off + ns_max, kAlign);
+  p->ns_bytes = ns_max;
+  if (p->cfg.offload) {
+    p->n_slots = std::max(1, std::min(2, (int)p->cfg.max_inflight)) + 1;
+    p->slot_bytes = align_up((size_t)p->max_elems * grad_size(p->cfg), kAlign) +
+                    2 * align_up((size_t)p->max_elems * 4, kAlign);
+    p->off_stage = off;
+    off += (size_t)p->n_slots * p->slot_bytes;
+  }
+  p->ws_bytes = align_up(off, kAlign);
+  return MUON_OK;
+}
+
+// ---------------------------------------------------------------------------
+// kernel argument assembly
+// ---------------------------------------------------------------------------
+template <typename T>
+T* at(const muon_plan_t* p, size_t off) { return reinterpret_cast<T*>(p->ws + off); }
+
+struct RunPtrs {  // where a run's G / M / W (or U') live for this call
+  const void* g;
+  float* m;
+  void* w;
+  int64_t stride;  // elements between consecutive matrices at those pointers
+};
+
+// Fills PrepArgs for bucket b; ptr(ti, first) gives the run's pointers.
+template <typename F>
+void make_prep_args(const muon_plan_t* p, const Bucket& b, F ptr, float mu, int nesterov, PrepArgs& a) {
+  std::memset(&a, 0, sizeof(a));
+  const bool tf32 = p->cfg.ns_precision == MUON_NS_TF32X3;
+  const size_t es = elem_size_ns(p->cfg);
+  int si = 0;
+  int64_t tile = 0;
+  for (const BGroup& g : b.groups) {
+    int64_t mat = g.mat_base;
+    for (const Run& r : g.runs) {
+      const TensorInfo& t = p->tensors[r.tensor];
+      PrepSeg& s = a.seg[si++];
+      RunPtrs rp = ptr(r);
+      s.g = rp.g;
+      s.m = rp.m;
+      const int64_t xoff = (mat - g.mat_base) * g.m * g.ld_n;
+      s.x_hi = p->ws + p->off_ns + g.off_x[0] + xoff * es;
+      s.x_lo = tf32 ? reinterpret_cast<float*>(p->ws + p->off_ns + g.off_x_lo[0]) + xoff : nullptr;
+      s.rows = t.rows; s.cols = t.cols;
+      s.stride = rp.stride;
+      s.x_ld = g.ld_n;
+      s.x_mstride = g.m * g.ld_n;
+      s.block0 = tile;
+      s.count = (int32_t)r.count;
+      s.transposed = t.transposed ? 1 : 0;
+      s.tiles_c = (int32_t)cdiv(t.cols, kPrepTile);
+      s.tiles_per_mat = (int32_t)tiles_of(t.rows, t.cols);
+      s.mat0 = (int32_t)mat;
+      tile += r.count * s.tiles_per_mat;
+      mat += r.count;
+    }
+  }
+  a.n_segs = si;
+  a.n_mats = (int32_t)b.n_mats;
+  a.total_tiles = tile;
+  const bool sgd = p->cfg.momentum_form == MUON_MOMENTUM_SGD;
+  a.mu = mu;
+  a.omu = sgd ? 1.0f : 1.0f - mu;
+  a.nesterov = nesterov ? 1 : 0;
+  a.grad_dtype = p->cfg.grad_dtype;
+  a.tf32 = tf32 ? 1 : 0;
+  a.eps = p->cfg.eps;
+  a.partials = at<float>(p, p->off_partials);
+  a.scale = at<float>(p, p->off_scale);
+  a.flags = at<int32_t>(p, p->off_flags);
+  a.status = at<DeviceStatus>(p, p->off_status);
+}
+
+template <typename F>
+void make_apply_args(const muon_plan_t* p, const Bucket& b, F ptr, int final_buf, float lr, float wd,
+                     int emit, int ns_steps, ApplyArgs& a) {
+  std::memset(&a, 0, sizeof(a));
+  const bool tf32 = p->cfg.ns_precision == MUON_NS_TF32X3;
+  const size_t es = elem_size_ns(p->cfg);
+  int si = 0;
+  int64_t tile = 0;
+  for (const BGroup& g : b.groups) {
+    int64_t mat = g.mat_base;
+    for (const Run& r : g.runs) {
+      const TensorInfo& t = p->tensors[r.tensor];
+      ApplySeg& s = a.seg[si++];
+      RunPtrs rp = ptr(r);
+      s.w = rp.w;
+      const int64_t xoff = (mat - g.mat_base) * g.m * g.ld_n;
+      s.u_hi = p->ws + p->off_ns + g.off_x[final_buf] + xoff * es;
+      s.u_lo = tf32 ? reinterpret_cast<const float*>(p->ws + p->off_ns + g.off_x_lo[final_buf]) + xoff : nullptr;
+      s.rows = t.rows; s.cols = t.cols;
+      s.stride = rp.stride;
+      s.u_ld = g.ld_n;
+      s.u_mstride = g.m * g.ld_n;
+      s.block0 = tile;
+      s.count = (int32_t)r.count;
+      s.transposed = t.transposed ? 1 : 0;
+      s.tiles_c = (int32_t)cdiv(t.cols, kPrepTile);
+      s.tiles_per_mat = (int32_t)tiles_of(t.rows, t.cols);
+      s.mat0 = (int32_t)mat;
+      s.shape_scale = (float)std::sqrt(std::max(1.0, (double)t.rows / (double)t.cols));
+      tile += r.count * s.tiles_per_mat;
+      mat += r.count;
+    }
+  }
+  a.n_segs = si;
+  a.total_tiles = tile;
+  a.lr = lr;
+  a.wd = wd;
+  a.param_dtype = p->cfg.param_dtype;
+  a.tf32 = tf32 ? 1 : 0;
+  a.emit = emit;
+  a.skip_nonfinite = p->cfg.skip_nonfinite;
+  a.unnormalized = ns_steps == 0 ? 1 : 0;
+  a.scale = at<float>(p, p->off_scale);
+  a.flags = at<int32_t>(p, p->off_flags);
+}
+
+int64_t sym_tiles_per_mat(int64_t M) {
+  const int64_t tm = cdiv(M, kBM), tn = cdiv(M, kBN);
+  int64_t total = 0;
+  for (int64_t bj = 0; bj < tn; ++bj) total += std::min(tm, (bj * kBN + kBN - 1) / kBM + 1);
+  return total;
+}
+
+muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st) {
+  const muon_config& c = p->cfg;
+  const bool tf32 = c.ns_precision == MUON_NS_TF32X3;
+  for (int it = 0; it < ns_steps; ++it) {
+    const int cur = it & 1, nxt = cur ^ 1;
+    for (int mode = kGram; mode <= kUpdate; ++mode) {
+      GemmArgs ga;
+      std::memset(&ga, 0, sizeof(ga));
+      ga.mode = mode;
+      ga.n_groups = (int32_t)b.groups.size();
+      ga.use_scale = it == 0 && mode != kPoly ? 1 : 0;
+      ga.alpha = mode == kPoly ? c.ns_c : 1.0f;
+      ga.beta = mode == kPoly ? c.ns_b : (mode == kUpdate ? c.ns_a : 0.0f);
+      ga.scale = at<float>(p, p->off_scale);
+      ga.status = at<DeviceStatus>(p, p->off_status);
+      int tiles = 0;
+      for (size_t gi = 0; gi < b.groups.size(); ++gi) {
+        const BGroup& g = b.groups[gi];
+        GemmGroup& G = ga.g[gi];
+        uint8_t* ns = p->ws + p->off_ns;
+        G.count = (int32_t)g.count;
+        G.mat_base = (int32_t)g.mat_base;
+        if (mode == kGram) {
+          G.map_a = g.kx[cur]; G.map_b = g.kx[cur];
+          G.c_hi = ns + g.off_a; G.d_hi = nullptr;
+          G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
+          G.M = (int32_t)g.m; G.N = (int32_t)g.m; G.K = (int32_t)g.n;
+        } else if (mode == kPoly) {
+          G.map_a = g.ka; G.map_b = g.ka;
+          G.c_hi = ns + g.off_b; G.d_hi = ns + g.off_a;
+          G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
+          G.M = (int32_t)g.m; G.N = (int32_t)g.m; G.K = (int32_t)g.m;
+        } else {
+          G.map_a = g.kb; G.map_b = g.mx[cur];
+          G.c_hi = ns + g.off_x[nxt]; G.d_hi = ns + g.off_x[cur];
+          G.c_ld = g.ld_n; G.c_mstride = g.m * g.ld_n;
+          G.M = (int32_t)g.m; G.N = (int32_t)g.n; G.K = (int32_t)g.m;
+        }
+        G.tiles_m = (int32_t)cdiv(G.M, kBM);
+        G.tiles_n = (int32_t)cdiv(G.N, kBN);
+        G.tiles_per_mat = mode == kUpdate ? G.tiles_m * G.tiles_n : (int32_t)sym_tiles_per_mat(G.M);
+        G.tile0 = tiles;
+        tiles += G.tiles_per_mat * G.count;
+      }
+      ga.total_tiles = tiles;
+      cudaError_t e = launch_gemm(ga, p->num_sms, tf32, st);
+      if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
+    }
+  }
+  return MUON_OK;
+}
+
+muon_status check_device_ptr(const void* ptr, const char* what, int i) {
+  if (ptr == nullptr) return fail(MUON_ERR_INVALID, "%s[%d] is NULL", what, i);
+  if (reinterpret_cast<uintptr_t>(ptr) & 15u) return fail(MUON_ERR_INVALID, "%s[%d] is not 16-byte aligned", what, i);
+  return MUON_OK;
+}
+
+muon_status check_pinned(const void* ptr, const char* what, int i) {
+  if (ptr == nullptr) return fail(MUON_ERR_INVALID, "%s[%d] is NULL", what, i);
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MUON_ERR_NOT_PINNED, "%s[%d] is not page-locked host memory", what, i);
+  }
+  if (attr.type != cudaMemoryTypeHost)
+    return fail(MUON_ERR_NOT_PINNED, "%s[%d] is not page-locked host memory", what, i);
+  return MUON_OK;
+}
+
+float elapsed(cudaEvent_t a, cudaEvent_t b) {
+  float ms = 0.f;
+  if (a && b && cudaEventElapsedTime(&ms, a, b) == cudaSuccess) return ms;
+  cudaGetLastError();
+  return 0.f;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char* muon_last_error(void) { return g_last_error.c_str(); }
+
+void muon_config_default(muon_config* cfg) {
+  if (!cfg) return;
+  std::memset(cfg, 0, sizeof(*cfg));
+  cfg->ns_a = 3.4445f;
+  cfg->ns_b = -4.7750f;
+  cfg->ns_c = 2.0315f;
+  cfg->eps = 1e-7f;
+  cfg->ns_precision = MUON_NS_BF16;
+  cfg->momentum_form = MUON_MOMENTUM_EMA;
+  cfg->grad_dtype = MUON_DTYPE_BF16;
+  cfg->param_dtype = MUON_DTYPE_F32;
+  cfg->max_inflight = 1;
+  cfg->skip_nonfinite = 1;
+  cfg->timing = 0;
+  cfg->offload = 0;
+}
+
+muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t* groups, int64_t bucket_cap_bytes,
+                      const muon_config* cfg, muon_plan_t** out) {
+  if (!out) return fail(MUON_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  if (!shapes || n_shapes <= 0) return fail(MUON_ERR_INVALID, "need at least one shape");
+  muon_config c;
+  if (cfg) c = *cfg; else muon_config_default(&c);
+  if (c.ns_precision != MUON_NS_BF16 && c.ns_precision != MUON_NS_TF32X3)
+    return fail(MUON_ERR_INVALID, "ns_precision must be MUON_NS_BF16 or MUON_NS_TF32X3");
+  if (c.momentum_form != MUON_MOMENTUM_EMA && c.momentum_form != MUON_MOMENTUM_SGD)
+    return fail(MUON_ERR_INVALID, "momentum_form must be EMA or SGD");
+  if (c.grad_dtype != MUON_DTYPE_BF16 && c.grad_dtype != MUON_DTYPE_F32)
+    return fail(MUON_ERR_INVALID, "grad_dtype must be BF16 or F32");
+  if (c.param_dtype != MUON_DTYPE_BF16 && c.param_dtype != MUON_DTYPE_F32)
+    return fail(MUON_ERR_INVALID, "param_dtype must be BF16 or F32");
+  if (!(c.eps >= 0.f) || !std::isfinite(c.ns_a) || !std::isfinite(c.ns_b) || !std::isfinite(c.ns_c))
+    return fail(MUON_ERR_INVALID, "eps must be >= 0 and coefficients finite");
+  if (c.max_inflight < 1 || c.max_inflight > 2) return fail(MUON_ERR_INVALID, "max_inflight must be 1 or 2");
+  muon_plan_t* p = new (std::nothrow) muon_plan_t();
+  if (!p) return fail(MUON_ERR_INVALID, "out of host memory");
+  p->cfg = c;
+  p->cap = bucket_cap_bytes;
+  muon_status s = build_plan(p, shapes, n_shapes, groups);
+  if (s != MUON_OK) {
+    delete p;
+    return s;
+  }
+  *out = p;
+  return MUON_OK;
+}
+
+muon_status muon_plan_workspace_bytes(const muon_plan_t* plan, size_t* device_bytes) {
+  if (!plan || !device_bytes) return fail(MUON_ERR_INVALID, "NULL argument");
+  *device_bytes = plan->ws_bytes;
+  return MUON_OK;
+}
+
+muon_status muon_get_plan_info(const muon_plan_t* plan, muon_plan_info* info) {
+  if (!plan || !info) return fail(MUON_ERR_INVALID, "NULL argument");
+  std::memset(info, 0, sizeof(*info));
+  info->n_tensors = (int64_t)plan->tensors.size();
+  info->n_matrices = plan->n_matrices;
+  info->n_groups = plan->n_groups;
+  info->n_buckets = (int64_t)plan->buckets.size();
+  for (const Bucket& b : plan->buckets) {
+    info->max_bucket_matrices = std::max(info->max_bucket_matrices, b.n_mats);
+    info->max_bucket_bytes = std::max(info->max_bucket_bytes, b.bytes);
+  }
+  info->workspace_bytes = plan->ws_bytes;
+  return MUON_OK;
+}
+
+muon_status muon_get_bucket_info(const muon_plan_t* plan, int64_t b, muon_bucket_info* info) {
+  if (!plan || !info) return fail(MUON_ERR_INVALID, "NULL argument");
+  if (b < 0 || b >= (int64_t)plan->buckets.size()) return fail(MUON_ERR_INVALID, "bucket index out of range");
+  const Bucket& k = plan->buckets[b];
+  info->n_matrices = k.n_mats;
+  info->bytes = k.bytes;
+  info->n_groups = (int64_t)k.groups.size();
+  info->m = k.groups[0].m;
+  info->n = k.groups[0].n;
+  return MUON_OK;
+}
+
+muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes) {
+  if (!p || !dev_ptr) return fail(MUON_ERR_INVALID, "NULL argument");
+  if (reinterpret_cast<uintptr_t>(dev_ptr) & 255u) return fail(MUON_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (bytes < p->ws_bytes)
+    return fail(MUON_ERR_NO_WORKSPACE, "workspace of %zu bytes is smaller than the %zu the plan needs", bytes,
+                p->ws_bytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (major != 10 || minor != 3)
+    return fail(MUON_ERR_UNSUPPORTED, "libmuon is built for sm_103a; device is sm_%d%d", major, minor);
+  cudaPointerAttributes attr;
+  e = cudaPointerGetAttributes(&attr, dev_ptr);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    return fail(MUON_ERR_INVALID, "workspace is not device memory");
+  }
+  if (!get_encode_fn()) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  p->ws = static_cast<uint8_t*>(dev_ptr);
+  p->ws_size = bytes;
+  p->device = dev;
+  p->num_sms = sms;
+  const size_t es = elem_size_ns(p->cfg);
+  const bool tf32 = p->cfg.ns_precision == MUON_NS_TF32X3;
+  const uint32_t kbox = tf32 ? 32 : 64;  // 128-byte rows
+  for (Bucket& b : p->buckets) {
+    for (BGroup& g : b.groups) {
+      uint8_t* ns = p->ws + p->off_ns;
+      bool ok = true;
+      for (int i = 0; i < 2; ++i) {
+        ok &= encode_map(&g.kx[i], ns + g.off_x[i], es, g.n, g.m, g.count, g.ld_n, kbox, 128);
+        ok &= encode_map(&g.mx[i], ns + g.off_x[i], es, g.n, g.m, g.count, g.ld_n, kbox, kbox);
+      }
+      ok &= encode_map(&g.ka, ns + g.off_a, es, g.m, g.m, g.count, g.ld_m, kbox, 128);
+      ok &= encode_map(&g.kb, ns + g.off_b, es, g.m, g.m, g.count, g.ld_m, kbox, 128);
+      if (!ok) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled rejected a workspace tensor map");
+    }
+  }
+  if (!p->h2d_stream) {
+    e = cudaStreamCreateWithFlags(&p->h2d_stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreate");
+    e = cudaStreamCreateWithFlags(&p->d2h_stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreate");
+    p->events.resize(p->buckets.size());
+    for (BucketEvents& ev : p->events) {
+      cudaEvent_t* all[] = {&ev.start, &ev.prep, &ev.ns, &ev.apply, &ev.h2d, &ev.d2h_start, &ev.d2h};
+      for (cudaEvent_t* x : all)
+        if ((e = cudaEventCreate(x)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+    }
+    const int slots = std::max(p->n_slots, 1);
+    p->slot_h2d.resize(slots); p->slot_comp.resize(slots); p->slot_d2h.resize(slots);
+    for (int i = 0; i < slots; ++i) {
+      cudaEventCreateWithFlags(&p->slot_h2d[i], cudaEventDisableTiming);
+      cudaEventCreateWithFlags(&p->slot_comp[i], cudaEventDisableTiming);
+      cudaEventCreateWithFlags(&p->slot_d2h[i], cudaEventDisableTiming);
+    }
+    cudaEventCreate(&p->step_start);
+    cudaEventCreate(&p->step_end);
+  }
+  e = cudaMemset(p->ws + p->off_status, 0, sizeof(DeviceStatus));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  return MUON_OK;
+}
+
+muon_status muon_step(muon_plan_t* p, void* const* params, const void* const* grads, void* const* momentum,
+                      int64_t n_mats, float lr, float mu, int32_t nesterov, float wd, int32_t ns_steps, void* stream) {
+  if (!p) return fail(MUON_ERR_INVALID, "plan is NULL");
+  if (!p->ws) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
+  if (!params || !grads || !momentum) return fail(MUON_ERR_INVALID, "pointer array is NULL");
+  if (n_mats != (int64_t)p->tensors.size())
+    return fail(MUON_ERR_INVALID, "n_mats %lld != %zu tensors in the plan", (long long)n_mats, p->tensors.size());
+  if (ns_steps < 0 || ns_steps > 16) return fail(MUON_ERR_INVALID, "ns_steps must be in [0, 16]");
+  if (!std::isfinite(lr) || !std::isfinite(mu) || !std::isfinite(wd)) return fail(MUON_ERR_INVALID, "lr, mu, wd must be finite");
+  if (p->cfg.ns_precision == MUON_NS_TF32X3) return fail(MUON_ERR_UNSUPPORTED, "3xTF32 Newton-Schulz is not built yet");
+  for (int i = 0; i < n_mats; ++i) {
+    muon_status s;
+    if ((s = check_device_ptr(params[i], "params", i)) != MUON_OK) return s;
+    if ((s = check_device_ptr(grads[i], "grads", i)) != MUON_OK) return s;
+    if ((s = check_device_ptr(momentum[i], "momentum", i)) != MUON_OK) return s;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool timing = p->cfg.timing != 0;
+  const size_t gs = grad_size(p->cfg), ps = param_size(p->cfg);
+  if (timing) cudaEventRecord(p->step_start, st);
+  for (size_t bi = 0; bi < p->buckets.size(); ++bi) {
+    const Bucket& b = p->buckets[bi];
+    auto ptrs = [&](const Run& r) {
+      const TensorInfo& t = p->tensors[r.tensor];
+      RunPtrs rp;
+      rp.g = static_cast<const uint8_t*>(grads[r.tensor]) + (size_t)r.first * t.stride * gs;
+      rp.m = static_cast<float*>(momentum[r.tensor]) + (size_t)r.first * t.stride;
+      rp.w = static_cast<uint8_t*>(params[r.tensor]) + (size_t)r.first * t.stride * ps;
+      rp.stride = t.stride;
+      return rp;
+    };
+    PrepArgs pa;
+    make_prep_args(p, b, ptrs, mu, nesterov, pa);
+    if (timing) cudaEventRecord(p->events[bi].start, st);
+    cudaError_t e = launch_prep(pa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "momentum_prep launch");
+    e = launch_norm(pa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
+    if (timing) cudaEventRecord(p->events[bi].prep, st);
+    muon_status s = enqueue_ns(p, b, ns_steps, st);
+    if (s != MUON_OK) return s;
+    if (timing) cudaEventRecord(p->events[bi].ns, st);
+    ApplyArgs aa;
+    make_apply_args(p, b, ptrs, ns_steps & 1, lr, wd, 0, ns_steps, aa);
+    e = launch_apply(aa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+    if (timing) cudaEventRecord(p->events[bi].apply, st);
+  }
+  if (timing) cudaEventRecord(p->step_end, st);
+  p->offload_last = false;
+  p->last_h2d_bytes = p->last_d2h_bytes = 0;
+  return MUON_OK;
+}
+
+muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* const* h_momentum,
+                              void* const* h_update_out, int64_t n_mats, float mu, int32_t nesterov,
+                              int32_t ns_steps, void* compute, void* copy, int64_t timeout_ms) {
+  if (!p) return fail(MUON_ERR_INVALID, "plan is NULL");
+  if (!p->ws) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
+  if (!p->cfg.offload || p->n_slots < 2)
+    return fail(MUON_ERR_NO_WORKSPACE, "plan was made without cfg.offload = 1 (no staging slots)");
+  if (!h_grads || !h_momentum || !h_update_out) return fail(MUON_ERR_INVALID, "pointer array is NULL");
+  if (n_mats != (int64_t)p->tensors.size())
+    return fail(MUON_ERR_INVALID, "n_mats %lld != %zu tensors in the plan", (long long)n_mats, p->tensors.size());
+  if (ns_steps < 0 || ns_steps > 16) return fail(MUON_ERR_INVALID, "ns_steps must be in [0, 16]");
+  if (p->cfg.ns_precision == MUON_NS_TF32X3) return fail(MUON_ERR_UNSUPPORTED, "3xTF32 Newton-Schulz is not built yet");
+  if (timeout_ms <= 0) return fail(MUON_ERR_INVALID, "timeout_ms must be > 0");
+  for (int i = 0; i < n_mats; ++i) {
+    muon_status s;
+    if ((s = check_pinned(h_grads[i], "h_grads", i)) != MUON_OK) return s;
+    if ((s = check_pinned(h_momentum[i], "h_momentum", i)) != MUON_OK) return s;
+    if ((s = check_pinned(h_update_out[i], "h_update_out", i)) != MUON_OK) return s;
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(compute);
+  cudaStream_t ds = copy ? static_cast<cudaStream_t>(copy) : p->d2h_stream;
+  cudaStream_t hs = p->h2d_stream;
+  const size_t gs = grad_size(p->cfg);
+  const bool timing = p->cfg.timing != 0;
+  int64_t h2d_bytes = 0, d2h_bytes = 0;
+  cudaError_t e;
+  if (timing) cudaEventRecord(p->step_start, cs);
+  // the host buffers must not be touched by the previous step any more
+  e = cudaEventRecord(p->slot_h2d[0], cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  cudaStreamWaitEvent(hs, p->slot_h2d[0], 0);
+  for (size_t bi = 0; bi < p->buckets.size(); ++bi) {
+    const Bucket& b = p->buckets[bi];
+    const int slot = (int)(bi % p->n_slots);
+    uint8_t* sbase = p->ws + p->off_stage + (size_t)slot * p->slot_bytes;
+    uint8_t* sg = sbase;
+    float* sm = reinterpret_cast<float*>(sbase + align_up((size_t)p->max_elems * gs, kAlign));
+    float* su = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sm) + align_up((size_t)p->max_elems * 4, kAlign));
+    if (bi >= (size_t)p->n_slots) cudaStreamWaitEvent(hs, p->slot_d2h[slot], 0);
+    if (timing) cudaEventRecord(p->events[bi].start, hs);
+    // host -> device: G and M of every run, packed contiguously in bucket order
+    std::vector<std::tuple<const Run*, int64_t>> run_off;
+    int64_t eoff = 0;
+    for (const BGroup& g : b.groups)
+      for (const Run& r : g.runs) {
+        const TensorInfo& t = p->tensors[r.tensor];
+        const int64_t me = t.rows * t.cols;
+        const uint8_t* hg = static_cast<const uint8_t*>(h_grads[r.tensor]) + (size_t)r.first * t.stride * gs;
+        const uint8_t* hm = static_cast<const uint8_t*>(h_momentum[r.tensor]) + (size_t)r.first * t.stride * 4;
+        e = cudaMemcpy2DAsync(sg + (size_t)eoff * gs, me * gs, hg, t.stride * gs, me * gs, r.count,
+                              cudaMemcpyHostToDevice, hs);
+        if (e == cudaSuccess)
+          e = cudaMemcpy2DAsync(sm + eoff, me * 4, hm, t.stride * 4, me * 4, r.count, cudaMemcpyHostToDevice, hs);
+        if (e != cudaSuccess) return cuda_fail(e, "host->device copy");
+        h2d_bytes += r.count * me * (int64_t)(gs + 4);
+        run_off.emplace_back(&r, eoff);
+        eoff += r.count * me;
+      }
+    cudaEventRecord(p->slot_h2d[slot], hs);
+    if (timing) cudaEventRecord(p->events[bi].h2d, hs);
+    cudaStreamWaitEvent(cs, p->slot_h2d[slot], 0);
+    // compute: prep (reads the staged G/M, writes M_new in place), NS, emit U'
+    auto stage_ptrs = [&](const Run& r) {
+      RunPtrs rp;
+      int64_t off = 0;
+      for (auto& ro : run_off)
+        if (std::get<0>(ro) == &r) off = std::get<1>(ro);
+      rp.g = sg + (size_t)off * gs;
+      rp.m = sm + off;
+      rp.w = su + off;
+      rp.stride = p->tensors[r.tensor].rows * p->tensors[r.tensor].cols;
+      return rp;
+    };
+    PrepArgs pa;
+    make_prep_args(p, b, stage_ptrs, mu, nesterov, pa);
+    if (timing) cudaEventRecord(p->events[bi].prep, cs);  // marks compute start for this bucket
+    if ((e = launch_prep(pa, cs)) != cudaSuccess) return cuda_fail(e, "momentum_prep launch");
+    if ((e = launch_norm(pa, cs)) != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
+    muon_status s = enqueue_ns(p, b, ns_steps, cs);
+    if (s != MUON_OK) return s;
+    if (timing) cudaEventRecord(p->events[bi].ns, cs);
+    ApplyArgs aa;
+    make_apply_args(p, b, stage_ptrs, ns_steps & 1, 0.f, 0.f, 1, ns_steps, aa);
+    if ((e = launch_apply(aa, cs)) != cudaSuccess) return cuda_fail(e, "emit launch");
+    cudaEventRecord(p->slot_comp[slot], cs);
+    if (timing) cudaEventRecord(p->events[bi].apply, cs);
+    // device -> host writeback on the side stream
+    cudaStreamWaitEvent(ds, p->slot_comp[slot], 0);
+    if (timing) cudaEventRecord(p->events[bi].d2h_start, ds);
+    for (auto& ro : run_off) {
+      const Run& r = *std::get<0>(ro);
+      const int64_t off = std::get<1>(ro);
+      const TensorInfo& t = p->tensors[r.tensor];
+      const int64_t me = t.rows * t.cols;
+      uint8_t* hm = static_cast<uint8_t*>(h_momentum[r.tensor]) + (size_t)r.first * t.stride * 4;
+      uint8_t* hu = static_cast<uint8_t*>(h_update_out[r.tensor]) + (size_t)r.first * t.stride * 4;
+      e = cudaMemcpy2DAsync(hm, t.stride * 4, sm + off, me * 4, me * 4, r.count, cudaMemcpyDeviceToHost, ds);
+      if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(hu, t.stride * 4, su + off, me * 4, me * 4, r.count, cudaMemcpyDeviceToHost, ds);
+      if (e != cudaSuccess) return cuda_fail(e, "device->host copy");
+      d2h_bytes += r.count * me * 8;
+    }
+    cudaEventRecord(p->slot_d2h[slot], ds);
+    if (timing) cudaEventRecord(p->events[bi].d2h, ds);
+  }
+  if (timing) cudaEventRecord(p->step_end, ds);
+  // drain: the host reads the results next
+  const auto t0 = std::chrono::steady_clock::now();
+  for (int sidx = 0; sidx < p->n_slots && sidx < (int)p->buckets.size(); ++sidx) {
+    for (;;) {
+      e = cudaEventQuery(p->slot_d2h[sidx]);
+      if (e == cudaSuccess) break;
+      if (e != cudaErrorNotReady) return cuda_fail(e, "writeback");
+      if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(timeout_ms))
+        return fail(MUON_ERR_TIMEOUT, "writeback did not finish within %lld ms", (long long)timeout_ms);
+      std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+  }
+  p->offload_last = true;
+  p->last_h2d_bytes = h2d_bytes;
+  p->last_d2h_bytes = d2h_bytes;
+  return MUON_OK;
+}
+
+muon_status muon_sync(muon_plan_t* p, void* stream, int64_t* n_nonfinite) {
+  if (!p) return fail(MUON_ERR_INVALID, "plan is NULL");
+  if (n_nonfinite) *n_nonfinite = 0;
+  if (!p->ws) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  DeviceStatus ds;
+  e = cudaMemcpy(&ds, p->ws + p->off_status, sizeof(ds), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  e = cudaMemset(p->ws + p->off_status, 0, sizeof(ds));
+  if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  if (n_nonfinite) *n_nonfinite = ds.nonfinite;
+  if (ds.flags) return fail(MUON_ERR_DEVICE, "a kernel gave up a bounded wait (status 0x%x)", ds.flags);
+  if (ds.nonfinite) return MUON_WARN_NONFINITE;
+  return MUON_OK;
+}
+
+muon_status muon_get_stats(const muon_plan_t* p, muon_stats* out) {
+  if (!p || !out) return fail(MUON_ERR_INVALID, "NULL argument");
+  std::memset(out, 0, sizeof(*out));
+  if (!p->cfg.timing) return fail(MUON_ERR_INVALID, "plan was made with timing = 0");
+  if (!p->step_end) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
+  cudaError_t e = cudaEventSynchronize(p->step_end);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+  for (size_t i = 0; i < p->buckets.size(); ++i) {
+    const BucketEvents& ev = p->events[i];
+    if (p->offload_last) {
+      out->h2d_ms += elapsed(ev.start, ev.h2d);
+      out->ns_ms += elapsed(ev.prep, ev.ns);
+      out->apply_ms += elapsed(ev.ns, ev.apply);
+      out->d2h_ms += elapsed(ev.d2h_start, ev.d2h);
+    } else {
+      out->prep_ms += elapsed(ev.start, ev.prep);
+      out->ns_ms += elapsed(ev.prep, ev.ns);
+      out->apply_ms += elapsed(ev.ns, ev.apply);
+    }
+  }
+  out->step_ms = elapsed(p->step_start, p->step_end);
+  out->h2d_bytes = p->last_h2d_bytes;
+  out->d2h_bytes = p->last_d2h_bytes;
+  out->n_buckets = (int64_t)p->buckets.size();
+  return MUON_OK;
+}
+
+const char* muon_status_string(muon_status s) {
+  switch (s) {
+    case MUON_OK: return "ok";
+    case MUON_WARN_NONFINITE: return "warning: non-finite matrix norm";
+    case MUON_ERR_INVALID: return "invalid argument";
+    case MUON_ERR_NOT_PINNED: return "host buffer is not page-locked";
+    case MUON_ERR_NO_WORKSPACE: return "no or too small workspace";
+    case MUON_ERR_CUDA: return "CUDA error";
+    case MUON_ERR_TIMEOUT: return "timed out";
+    case MUON_ERR_UNSUPPORTED: return "unsupported";
+    case MUON_ERR_DEVICE: return "device-side bounded wait ran out";
+    default: return "unknown status";
+  }
+}
+
+void muon_plan_destroy(muon_plan_t* p) {
+  if (!p) return;
+  if (p->h2d_stream) {
+    for (BucketEvents& ev : p->events) {
+      cudaEvent_t all[] = {ev.start, ev.prep, ev.ns, ev.apply, ev.h2d, ev.d2h_start, ev.d2h};
+      for (cudaEvent_t x : all)
+        if (x) cudaEventDestroy(x);
+    }
+    for (auto v : {&p->slot_h2d, &p->slot_comp, &p->slot_d2h})
+      for (cudaEvent_t x : *v)
+        if (x) cudaEventDestroy(x);
+    if (p->step_start) cudaEventDestroy(p->step_start);
+    if (p->step_end) cudaEventDestroy(p->step_end);
+    cudaStreamDestroy(p->h2d_stream);
+    cudaStreamDestroy(p->d2h_stream);
+  }
+  delete p;
+}
+
+}  // extern "C"

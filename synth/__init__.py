@@ -208,3 +208,68 @@ def as_f64(a: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == BF16:
         return bf16_bits_to_f32(a).astype(np.float64)
     return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# device fill (libmuonsynth.so, the CUDA twin of normal_f32 / f32_to_bf16_bits)
+# ---------------------------------------------------------------------------
+_LIB = None
+
+
+def _cuda_lib():
+    global _LIB
+    if _LIB is None:
+        import ctypes
+        import os
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmuonsynth.so")
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing; build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        lib.synth_fill_normal.restype = ctypes.c_int
+        lib.synth_fill_normal.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint32,
+                                          ctypes.c_uint32, ctypes.c_uint32, ctypes.c_float, ctypes.c_int32,
+                                          ctypes.c_void_p]
+        lib.synth_philox.restype = ctypes.c_int
+        lib.synth_philox.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                     ctypes.c_void_p]
+        _LIB = lib
+    return _LIB
+
+
+def fill_normal_cuda(t, seed: int, stream: int, step: int, sigma: float, start: int = 0,
+                     cuda_stream=None) -> None:
+    """Fill a contiguous torch CUDA tensor (float32 or bfloat16) with elements
+    [start, start + t.numel()) of the seeded tensor, bit-identical to ``tensor``."""
+    import ctypes
+    import torch
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("need a contiguous CUDA tensor")
+    if t.dtype == torch.float32:
+        code = F32
+    elif t.dtype == torch.bfloat16:
+        code = BF16
+    else:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    s = cuda_stream if cuda_stream is not None else torch.cuda.current_stream()
+    rc = _cuda_lib().synth_fill_normal(ctypes.c_void_p(t.data_ptr()), int(start), int(t.numel()),
+                                       int(seed) & 0xFFFFFFFF, int(stream) & 0xFFFFFFFF,
+                                       int(step) & 0xFFFFFFFF, float(sigma), code,
+                                       ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_normal failed with CUDA error {rc}")
+
+
+def philox_cuda(ctr, key):
+    """Raw Philox-4x32-10 on the device: ctr (n,4) and key (n,2) uint32 numpy arrays."""
+    import ctypes
+    import torch
+    n = ctr.shape[0]
+    c = torch.from_numpy(np.ascontiguousarray(ctr, dtype=np.uint32).view(np.int32)).cuda()
+    k = torch.from_numpy(np.ascontiguousarray(key, dtype=np.uint32).view(np.int32)).cuda()
+    out = torch.empty((n, 4), dtype=torch.int32, device="cuda")
+    rc = _cuda_lib().synth_philox(ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(c.data_ptr()),
+                                  ctypes.c_void_p(k.data_ptr()), n,
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if rc != 0:
+        raise RuntimeError(f"synth_philox failed with CUDA error {rc}")
+    return out.cpu().numpy().view(np.uint32)
