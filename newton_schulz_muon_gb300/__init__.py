@@ -4,8 +4,8 @@ Every function here has the name of the C entry point it calls (include/muon.h)
 and only marshals arguments: torch tensors become device pointers and
 ``cudaStream_t`` handles; every step of the method runs in the library's
 kernels.  PyTorch provides device memory (the workspace, the caller's tensors)
-and streams.  There is no fallback: if libmuon.so is missing this module fails
-to import.
+and streams.  There is no fallback: libmuon.so is loaded on first use and a
+missing library raises ImportError there.
 """
 from __future__ import annotations
 
@@ -94,14 +94,27 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-lib = _load()
+_LIB = None
+
+
+def _lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _lib()
+    raise AttributeError(name)
 
 
 class MuonError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        msg = lib.muon_last_error().decode() or lib.muon_status_string(status).decode()
-        super().__init__(f"{where}: {lib.muon_status_string(status).decode()} ({status}): {msg}")
+        msg = _lib().muon_last_error().decode() or _lib().muon_status_string(status).decode()
+        super().__init__(f"{where}: {_lib().muon_status_string(status).decode()} ({status}): {msg}")
 
 
 def _check(status: int, where: str) -> int:
@@ -113,7 +126,7 @@ def _check(status: int, where: str) -> int:
 def muon_config_default(**overrides) -> muon_config:
     """The library's default configuration, with fields overridden by keyword."""
     cfg = muon_config()
-    lib.muon_config_default(byref(cfg))
+    _lib().muon_config_default(byref(cfg))
     for k, v in overrides.items():
         if not hasattr(cfg, k):
             raise AttributeError(f"muon_config has no field {k!r}")
@@ -132,7 +145,7 @@ class Plan:
     def __del__(self):
         h = getattr(self, "handle", None)
         if h is not None and h.value:
-            lib.muon_plan_destroy(h)
+            _lib().muon_plan_destroy(h)
             self.handle = c_void_p(0)
 
 
@@ -162,21 +175,21 @@ def muon_plan(shapes: Sequence[Sequence[int]], groups: Optional[Sequence[int]] =
     if groups is not None:
         g = (c_int32 * n)(*[int(v) for v in groups])
     out = c_void_p()
-    _check(lib.muon_plan(arr, n, g, int(bucket_cap_bytes), byref(config) if config is not None else None,
+    _check(_lib().muon_plan(arr, n, g, int(bucket_cap_bytes), byref(config) if config is not None else None,
                          byref(out)), "muon_plan")
     return Plan(out.value, n)
 
 
 def muon_plan_workspace_bytes(plan: Plan) -> int:
     v = c_size_t()
-    _check(lib.muon_plan_workspace_bytes(plan.handle, byref(v)), "muon_plan_workspace_bytes")
+    _check(_lib().muon_plan_workspace_bytes(plan.handle, byref(v)), "muon_plan_workspace_bytes")
     return v.value
 
 
 def muon_plan_bind_workspace(plan: Plan, workspace) -> None:
     """workspace: a torch uint8 CUDA tensor of at least muon_plan_workspace_bytes bytes."""
     nbytes = workspace.numel() * workspace.element_size()
-    _check(lib.muon_plan_bind_workspace(plan.handle, c_void_p(workspace.data_ptr()), nbytes),
+    _check(_lib().muon_plan_bind_workspace(plan.handle, c_void_p(workspace.data_ptr()), nbytes),
            "muon_plan_bind_workspace")
     plan.workspace = workspace
 
@@ -184,7 +197,7 @@ def muon_plan_bind_workspace(plan: Plan, workspace) -> None:
 def muon_step(plan: Plan, params, grads, momentum, lr: float, mu: float, nesterov: bool, wd: float,
               ns_steps: int = 5, stream=None) -> None:
     n = len(params)
-    _check(lib.muon_step(plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), n, float(lr),
+    _check(_lib().muon_step(plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), n, float(lr),
                          float(mu), int(bool(nesterov)), float(wd), int(ns_steps), _stream_ptr(stream)),
            "muon_step")
 
@@ -192,7 +205,7 @@ def muon_step(plan: Plan, params, grads, momentum, lr: float, mu: float, nestero
 def muon_offload_step(plan: Plan, h_grads, h_momentum, h_update_out, mu: float, nesterov: bool,
                       ns_steps: int = 5, compute=None, copy=None, timeout_ms: int = 600_000) -> None:
     n = len(h_grads)
-    _check(lib.muon_offload_step(plan.handle, _ptrs(h_grads), _ptrs(h_momentum), _ptrs(h_update_out), n,
+    _check(_lib().muon_offload_step(plan.handle, _ptrs(h_grads), _ptrs(h_momentum), _ptrs(h_update_out), n,
                                  float(mu), int(bool(nesterov)), int(ns_steps), _stream_ptr(compute),
                                  c_void_p(int(getattr(copy, "cuda_stream", copy))) if copy is not None
                                  else c_void_p(0), int(timeout_ms)),
@@ -202,30 +215,30 @@ def muon_offload_step(plan: Plan, h_grads, h_momentum, h_update_out, mu: float, 
 def muon_sync(plan: Plan, stream=None):
     """Returns (status, n_nonfinite); raises on errors (a device wait that ran out)."""
     nf = c_int64()
-    st = _check(lib.muon_sync(plan.handle, _stream_ptr(stream), byref(nf)), "muon_sync")
+    st = _check(_lib().muon_sync(plan.handle, _stream_ptr(stream), byref(nf)), "muon_sync")
     return st, nf.value
 
 
 def muon_get_plan_info(plan: Plan) -> muon_plan_info:
     info = muon_plan_info()
-    _check(lib.muon_get_plan_info(plan.handle, byref(info)), "muon_get_plan_info")
+    _check(_lib().muon_get_plan_info(plan.handle, byref(info)), "muon_get_plan_info")
     return info
 
 
 def muon_get_bucket_info(plan: Plan, b: int) -> muon_bucket_info:
     info = muon_bucket_info()
-    _check(lib.muon_get_bucket_info(plan.handle, int(b), byref(info)), "muon_get_bucket_info")
+    _check(_lib().muon_get_bucket_info(plan.handle, int(b), byref(info)), "muon_get_bucket_info")
     return info
 
 
 def muon_get_stats(plan: Plan) -> muon_stats:
     st = muon_stats()
-    _check(lib.muon_get_stats(plan.handle, byref(st)), "muon_get_stats")
+    _check(_lib().muon_get_stats(plan.handle, byref(st)), "muon_get_stats")
     return st
 
 
 def muon_status_string(status: int) -> str:
-    return lib.muon_status_string(int(status)).decode()
+    return _lib().muon_status_string(int(status)).decode()
 
 
 def allocate_workspace(plan: Plan, device=None):

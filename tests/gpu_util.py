@@ -77,7 +77,10 @@ class Workload:
         self.W, self.M, self.G = [], [], []
         for i, (r, c, k) in enumerate(self.shapes):
             n = (k, r, c)
-            self.W.append(synth.tensor(seed, synth.stream_id(i, synth.ROLE_W), 0, n, w_sigma, w_dtype))
+            if w_sigma > 0:
+                self.W.append(synth.tensor(seed, synth.stream_id(i, synth.ROLE_W), 0, n, w_sigma, w_dtype))
+            else:
+                self.W.append(np.zeros(n, np.uint16 if w_dtype == synth.BF16 else np.float32))
             if m_sigma > 0:
                 self.M.append(synth.tensor(seed, synth.stream_id(i, synth.ROLE_M), 0, n, m_sigma, synth.F32))
             else:

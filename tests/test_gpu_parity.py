@@ -79,8 +79,10 @@ def test_single_256x512_three_steps(m):
 
 @pytest.mark.parametrize("coeffs", [(1.0, 0.0, 0.0), (0.0, 1.0, 0.0), (0.0, 0.0, 1.0), (0.5, -0.25, 0.125)])
 def test_one_iteration_isolates_each_gemm(m, coeffs):
-    # (1,0,0): UPDATE epilogue only; (0,1,0): GRAM + UPDATE; (0,0,1): GRAM + POLY + UPDATE
-    wl = Workload([(192, 320), (320, 192), (64, 640)], g_sigma=1.0, g_dtype=synth.F32)
+    # (1,0,0): UPDATE epilogue only; (0,1,0): GRAM + UPDATE; (0,0,1): GRAM + POLY + UPDATE.
+    # W starts at 0 so that the (tiny, for a monomial) update is not lost in the
+    # fp32 rounding of W.
+    wl = Workload([(192, 320), (320, 192), (64, 640)], w_sigma=0.0, g_sigma=1.0, g_dtype=synth.F32)
     _run(m, wl, ns_steps=1, coeffs=coeffs, mu=0.0, nesterov=False)
 
 
