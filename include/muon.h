@@ -158,6 +158,28 @@ muon_status muon_offload_step(muon_plan_t* plan, const void* const* h_grads,
                               int64_t n_mats, float mu, int32_t nesterov, int32_t ns_steps,
                               void* compute, void* copy, int64_t timeout_ms);
 
+/* muon_step for callers that cannot allocate device memory (code running inside
+ * an allocator or memory-pool callback, a runtime that has given all device
+ * memory to its own pool, a plugin host that forbids device allocations).  The
+ * sources describe no such variant; it has no counterpart there.
+ * Same arguments and results as muon_step, but no workspace is bound by the
+ * caller: the step runs in a file-scope device array of the library
+ * (muon_noalloc_scratch_bytes(), 64 MiB), which every GPU that loads the library
+ * holds until exit.  The entry point allocates nothing (no cudaMalloc/cudaFree,
+ * no allocating library routine).
+ *   - The first call on a device, with that device current, looks up the array's
+ *     address (cudaGetSymbolAddress); make it before any stream capture.
+ *   - Each call binds `plan` to the array (tensor maps, status word cleared).
+ *   - Plans whose workspace exceeds the array: MUON_ERR_NO_WORKSPACE.
+ *   - All calls share the array and it keeps the last call's contents: calls
+ *     whose device work overlaps race on it; serialise them. */
+muon_status muon_step_noalloc(muon_plan_t* plan, void* const* params, const void* const* grads,
+                              void* const* momentum, int64_t n_mats, float lr, float mu,
+                              int32_t nesterov, float wd, int32_t ns_steps, void* stream);
+
+/* Size in bytes of the static array muon_step_noalloc works in. */
+size_t muon_noalloc_scratch_bytes(void);
+
 /* Waits for `stream`, then reads and clears the device status word written by
  * the kernels: MUON_ERR_DEVICE if a kernel's bounded wait ran out,
  * MUON_WARN_NONFINITE (with *n_nonfinite set) if a matrix norm was not finite,

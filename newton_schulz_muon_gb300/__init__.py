@@ -86,6 +86,9 @@ def _load() -> ctypes.CDLL:
         "muon_last_error": (c_char_p, []),
         "muon_status_string": (c_char_p, [c_int32]),
         "muon_plan_destroy": (None, [P]),
+        "muon_step_noalloc": (c_int32, [P, POINTER(P), POINTER(P), POINTER(P), c_int64, c_float, c_float,
+                                        c_int32, c_float, c_int32, P]),
+        "muon_noalloc_scratch_bytes": (c_size_t, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -200,6 +203,21 @@ def muon_step(plan: Plan, params, grads, momentum, lr: float, mu: float, nestero
     _check(_lib().muon_step(plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), n, float(lr),
                          float(mu), int(bool(nesterov)), float(wd), int(ns_steps), _stream_ptr(stream)),
            "muon_step")
+
+
+def muon_step_noalloc(plan: Plan, params, grads, momentum, lr: float, mu: float, nesterov: bool,
+                      wd: float, ns_steps: int = 5, stream=None) -> None:
+    """muon_step without a caller-bound workspace, for callers that cannot allocate
+    device memory: the step runs in the library's static device scratch."""
+    n = len(params)
+    _check(_lib().muon_step_noalloc(plan.handle, _ptrs(params), _ptrs(grads), _ptrs(momentum), n,
+                                    float(lr), float(mu), int(bool(nesterov)), float(wd), int(ns_steps),
+                                    _stream_ptr(stream)),
+           "muon_step_noalloc")
+
+
+def muon_noalloc_scratch_bytes() -> int:
+    return int(_lib().muon_noalloc_scratch_bytes())
 
 
 def muon_offload_step(plan: Plan, h_grads, h_momentum, h_update_out, mu: float, nesterov: bool,

@@ -130,4 +130,7 @@ cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t s);
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, cudaStream_t s);
 size_t gemm_smem_bytes(bool tf32);
 
+// Records `msg` as the calling thread's muon_last_error text and returns `s`.
+int32_t set_error(int32_t s, const char* msg);
+
 }  // namespace muon

@@ -492,6 +492,8 @@ float elapsed(cudaEvent_t a, cudaEvent_t b) {
 
 }  // namespace
 
+int32_t muon::set_error(int32_t s, const char* msg) { return fail(s, "%s", msg); }
+
 // ===========================================================================
 // C ABI
 // ===========================================================================
