@@ -162,9 +162,19 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
     }
   }
 
-  // X0 = cast(V) in wide orientation (the 1/(||V||+eps) factor is applied later).
+  // X0 = cast(V) in wide orientation (the 1/(||V||+eps) factor is applied later);
+  // in 3xTF32 mode also X0^T, the layout the UPDATE GEMM reads.
   const int64_t xb = tile.mat * s.x_mstride;
-  if (!s.transposed) {
+  const bool need_vt = s.transposed || a.tf32;
+  if (need_vt) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vt[ty + 16 * k][4 * tx + j] = v[k][j];
+    __syncthreads();
+  }
+  // P[r][c] = V[r][c]
+  auto store_direct = [&](void* hi, float* lo, int64_t ld, int64_t base) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int64_t r = tile.r0 + ty + 16 * k;
@@ -175,24 +185,20 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
         uint2 raw;
         raw.x = *reinterpret_cast<uint32_t*>(&p0);
         raw.y = *reinterpret_cast<uint32_t*>(&p1);
-        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(s.x_hi) + xb + r * s.x_ld + c) = raw;
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(hi) + base + r * ld + c) = raw;
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (r < rows && c + j < cols) store_x(s.x_hi, s.x_lo, xb + r * s.x_ld + c + j, v[k][j], a.tf32);
+          if (r < rows && c + j < cols) store_x(hi, lo, base + r * ld + c + j, v[k][j], a.tf32);
       }
     }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) vt[ty + 16 * k][4 * tx + j] = v[k][j];
-    __syncthreads();
-    // X[c][r] = V[r][c]: X row = source column, X column = source row.
+  };
+  // P[c][r] = V[r][c]: P row = source column, P column = source row
+  auto store_transposed = [&](void* hi, float* lo, int64_t ld, int64_t base) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int xi = ty + 16 * k;        // source column within the tile
-      const int64_t xr = tile.c0 + xi;   // X row
+      const int xi = ty + 16 * k;
+      const int64_t xr = tile.c0 + xi;
       const int64_t xc = tile.r0 + 4 * tx;
       float w4[4];
 #pragma unroll
@@ -203,13 +209,20 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
         uint2 raw;
         raw.x = *reinterpret_cast<uint32_t*>(&p0);
         raw.y = *reinterpret_cast<uint32_t*>(&p1);
-        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(s.x_hi) + xb + xr * s.x_ld + xc) = raw;
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(hi) + base + xr * ld + xc) = raw;
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (xr < cols && xc + j < rows) store_x(s.x_hi, s.x_lo, xb + xr * s.x_ld + xc + j, w4[j], a.tf32);
+          if (xr < cols && xc + j < rows) store_x(hi, lo, base + xr * ld + xc + j, w4[j], a.tf32);
       }
     }
+  };
+  if (!s.transposed) store_direct(s.x_hi, s.x_lo, s.x_ld, xb);
+  else store_transposed(s.x_hi, s.x_lo, s.x_ld, xb);
+  if (a.tf32) {
+    const int64_t tb = tile.mat * s.xt_mstride;
+    if (!s.transposed) store_transposed(s.xt_hi, s.xt_lo, s.xt_ld, tb);
+    else store_direct(s.xt_hi, s.xt_lo, s.xt_ld, tb);
   }
 
   sumsq = warp_sum(sumsq);

@@ -32,6 +32,10 @@ struct PrepSeg {
   int64_t x_ld;          // leading dimension of X (wide form m x n)
   int64_t x_mstride;     // elements between consecutive matrices in X
   int64_t block0;        // first tile index of the run in the bucket's tile space
+  void* xt_hi;           // 3xTF32: X0^T (n x m) of the run's first matrix, else null
+  float* xt_lo;
+  int64_t xt_ld;         // leading dimension of X^T
+  int64_t xt_mstride;    // elements between consecutive matrices in X^T
   int32_t count;         // matrices in the run
   int32_t transposed;    // 1 when rows > cols: X = V^T
   int32_t tiles_c;       // 64-wide tiles along cols
@@ -91,7 +95,7 @@ enum GemmMode : int32_t { kGram = 0, kPoly = 1, kUpdate = 2 };
 
 struct GemmGroup {
   CUtensorMap map_a;     // operand A (K-major, box {64 (k), 128 rows})
-  CUtensorMap map_b;     // operand B (K-major box {64, 128} x2, or MN-major box {64, 64} x4)
+  CUtensorMap map_b;     // operand B (K-major box {64, 128} x2, or bf16 UPDATE: MN-major box {64, 64} x4)
   CUtensorMap map_a_lo;  // 3xTF32: low parts (unused in bf16 mode)
   CUtensorMap map_b_lo;
   void* c_hi;            // output (bf16 or tf32-hi fp32)
@@ -99,6 +103,9 @@ struct GemmGroup {
   const void* d_hi;      // epilogue addend (POLY: A, UPDATE: X)
   const float* d_lo;
   int64_t c_ld, c_mstride;   // elements
+  void* ct_hi;               // 3xTF32 UPDATE: also write the output transposed (X'^T), else null
+  float* ct_lo;
+  int64_t ct_ld, ct_mstride;
   int32_t M, N, K;           // output rows, cols, reduction length
   int32_t count;             // matrices
   int32_t tiles_m, tiles_n;  // tile grid of one matrix

@@ -11,19 +11,24 @@
 //   POLY   B  = c (A A) + b A    m x m, symmetric (a polynomial of A); A A is read
 //                                as A A^T so both operands are K-major rows; the
 //                                b A term is added in the epilogue.
-//   UPDATE X' = (B X) + a X      m x n; B rows are K-major, X is read MN-major
-//                                (n contiguous); the a X term is added in the
+//   UPDATE X' = (B X) + a X      m x n; B rows are K-major; bf16 reads X MN-major
+//                                (n contiguous); 3xTF32 reads the rows of X^T
+//                                (K-major, kept beside X in that mode) and also
+//                                writes X'^T.  The a X term is added in the
 //                                epilogue.
 //
 // In the first iteration X holds the un-normalised V; the per-matrix factor
 // s = 1/(||V||_F + eps) is applied in the epilogues (GRAM: s^2, UPDATE: s).
 //
 // Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0  lane 0: TMA producer over a 4-stage shared-memory ring
-//                   (A 128 x 64 bf16 + B 256 x 64 bf16 per stage, 128-byte swizzle)
-//   warp 1  lane 0: tcgen05.mma issuer, M=128 N=256 K=16, fp32 accumulators in
-//                   TMEM, two accumulator buffers (512 columns) so the epilogue of
-//                   one tile overlaps the main loop of the next
+//   warp 0  lane 0: TMA producer over a shared-memory ring of 128-byte-swizzled
+//                   stages: bf16 -- 4 stages of A 128 x 64 + B 256 x 64;
+//                   3xTF32 -- 2 stages of A 128 x 32 and B 256 x 32, each as a
+//                   tf32-high and a tf32-low fp32 copy
+//   warp 1  lane 0: tcgen05.mma issuer, M=128 N=256 (K=16 bf16 / K=8 tf32), fp32
+//                   accumulators in TMEM, two accumulator buffers (512 columns)
+//                   so the epilogue of one tile overlaps the main loop of the
+//                   next.  3xTF32 issues hi*hi + hi*lo + lo*hi per k step.
 //   warps 2-5:      epilogue; warp w reads TMEM lanes 32*(w%4)..+31 with
 //                   tcgen05.ld, applies alpha/beta, converts to bf16 and stores.
 // Tiles of all same-shape groups of a micro-bucket (and of all its matrices) are
@@ -39,14 +44,26 @@
 namespace muon {
 namespace {
 
-constexpr int kBK = 64;  // bf16 elements per 128-byte swizzle row
-constexpr int kStages = 4;
 constexpr int kThreadsG = 192;
-constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;   // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
+
+// Per-precision constants.  A "part" is one copy of an operand tile: bf16 has one,
+// 3xTF32 has a tf32-high and a tf32-low fp32 copy.  Rows are 128 bytes (one
+// swizzle atom wide), so a part of A is 16 KB and a part of B 32 KB in both modes.
+template <bool kTF32>
+struct Cfg {
+  static constexpr int kBK = kTF32 ? 32 : 64;           // k elements per 128-byte row
+  static constexpr int kStages = kTF32 ? 2 : 4;
+  static constexpr int kParts = kTF32 ? 2 : 1;
+  static constexpr uint32_t kA = kBM * 128;              // 16 KB
+  static constexpr uint32_t kB = kBN * 128;              // 32 KB
+  static constexpr uint32_t kStage = kParts * (kA + kB);
+  static constexpr int kInstK = kTF32 ? 8 : 16;          // k per MMA instruction
+  static constexpr int kChunks = kBN / kBK;              // MN-major: 128-byte column chunks per tile
+  static constexpr uint32_t kChunkBytes = kBK * 128;     // one chunk: kBK k-rows of 128 B
+  static constexpr uint32_t kFormat = kTF32 ? 2u : 1u;   // tf32 / bf16 in the instruction descriptor
+  static constexpr size_t kSmem = (size_t)kStages * kStage + 1024;
+};
 
 struct TileCoord {
   int g, b, bi, bj;
@@ -87,12 +104,122 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
-__global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid_constant__ GemmArgs a) {
+// ---------------------------------------------------------------------------
+// epilogue element access: 32 consecutive columns of one row
+// ---------------------------------------------------------------------------
+template <bool kTF32>
+struct Epi;
+
+template <>
+struct Epi<false> {  // bf16 storage
+  static __device__ __forceinline__ void add_d(float (&v)[32], const GemmGroup& G, int64_t off, bool full,
+                                               int64_t valid, float alpha, float beta) {
+    const __nv_bfloat16* drow = reinterpret_cast<const __nv_bfloat16*>(G.d_hi) + off;
+    if (full) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(drow + 8 * q);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w4[h]);
+          v[8 * q + 2 * h] = alpha * v[8 * q + 2 * h] + beta * __low2float(p);
+          v[8 * q + 2 * h + 1] = alpha * v[8 * q + 2 * h + 1] + beta * __high2float(p);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = alpha * v[j] + (j < valid ? beta * __bfloat162float(drow[j]) : 0.f);
+    }
+  }
+  // store columns [8q, 8q+8) of the chunk when `all8`, else the masked ones
+  static __device__ __forceinline__ void store8(const GemmGroup& G, int64_t off, const float* v, bool all8,
+                                                unsigned mask) {
+    __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(G.c_hi) + off;
+    if (all8) {
+      uint4 raw;
+      raw.x = pack_bf16x2(v[0], v[1]);
+      raw.y = pack_bf16x2(v[2], v[3]);
+      raw.z = pack_bf16x2(v[4], v[5]);
+      raw.w = pack_bf16x2(v[6], v[7]);
+      *reinterpret_cast<uint4*>(c) = raw;
+    } else {
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (mask & (1u << h)) c[h] = __float2bfloat16_rn(v[h]);
+    }
+  }
+  static __device__ __forceinline__ void store1(const GemmGroup& G, int64_t off, float v) {
+    reinterpret_cast<__nv_bfloat16*>(G.c_hi)[off] = __float2bfloat16_rn(v);
+  }
+};
+
+template <>
+struct Epi<true> {  // 3xTF32: fp32 tf32-high + fp32 low parts
+  static __device__ __forceinline__ void add_d(float (&v)[32], const GemmGroup& G, int64_t off, bool full,
+                                               int64_t valid, float alpha, float beta) {
+    const float* dh = reinterpret_cast<const float*>(G.d_hi) + off;
+    const float* dl = G.d_lo + off;
+    if (full) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 h = *reinterpret_cast<const float4*>(dh + 4 * q);
+        const float4 l = *reinterpret_cast<const float4*>(dl + 4 * q);
+        v[4 * q + 0] = alpha * v[4 * q + 0] + beta * (h.x + l.x);
+        v[4 * q + 1] = alpha * v[4 * q + 1] + beta * (h.y + l.y);
+        v[4 * q + 2] = alpha * v[4 * q + 2] + beta * (h.z + l.z);
+        v[4 * q + 3] = alpha * v[4 * q + 3] + beta * (h.w + l.w);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = alpha * v[j] + (j < valid ? beta * (dh[j] + dl[j]) : 0.f);
+    }
+  }
+  static __device__ __forceinline__ void store8(const GemmGroup& G, int64_t off, const float* v, bool all8,
+                                                unsigned mask) {
+    float* ch = reinterpret_cast<float*>(G.c_hi) + off;
+    float* cl = G.c_lo + off;
+    float hi[8], lo[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      hi[h] = round_tf32(v[h]);
+      lo[h] = v[h] - hi[h];
+    }
+    if (all8) {
+      *reinterpret_cast<float4*>(ch) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<float4*>(ch + 4) = make_float4(hi[4], hi[5], hi[6], hi[7]);
+      *reinterpret_cast<float4*>(cl) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<float4*>(cl + 4) = make_float4(lo[4], lo[5], lo[6], lo[7]);
+    } else {
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (mask & (1u << h)) {
+          ch[h] = hi[h];
+          cl[h] = lo[h];
+        }
+    }
+  }
+  static __device__ __forceinline__ void store1(const GemmGroup& G, int64_t off, float v) {
+    const float h = round_tf32(v);
+    reinterpret_cast<float*>(G.c_hi)[off] = h;
+    G.c_lo[off] = v - h;
+  }
+  // the transposed copy X'^T of the UPDATE output
+  static __device__ __forceinline__ void store1t(const GemmGroup& G, int64_t off, float v) {
+    const float h = round_tf32(v);
+    reinterpret_cast<float*>(G.ct_hi)[off] = h;
+    G.ct_lo[off] = v - h;
+  }
+};
+
+template <bool kTF32>
+__global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  using C = Cfg<kTF32>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full_bar[kStages];
-  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t full_bar[C::kStages];
+  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -105,7 +232,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -121,6 +248,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
     for (int i = 0; i < a.n_groups; ++i) {
       tma_prefetch_desc(&a.g[i].map_a);
       tma_prefetch_desc(&a.g[i].map_b);
+      if (kTF32) {
+        tma_prefetch_desc(&a.g[i].map_a_lo);
+        tma_prefetch_desc(&a.g[i].map_b_lo);
+      }
     }
   }
   if (warp == 1) {
@@ -132,6 +263,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
   const int mode = a.mode;
+  const bool mn_b = (mode == kUpdate) && !kTF32;  // B operand read MN-major
 
   if (warp == 0) {
     if (lane == 0) {
@@ -141,39 +273,44 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
       for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile(a, t);
         const GemmGroup& G = a.g[tc.g];
-        const int kblocks = (G.K + kBK - 1) / kBK;
+        const int kblocks = (G.K + C::kBK - 1) / C::kBK;
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_p, status)) { ok = false; break; }
-          uint8_t* sa = smem + (size_t)stage * kStageBytes;
-          uint8_t* sb = sa + kABytes;
-          mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-          const int k0 = kb * kBK;
-          tma_load_3d(sa, &G.map_a, &full_bar[stage], k0, tc.bi * kBM, tc.b);
-          if (mode == kUpdate) {
+          uint8_t* sa = smem + (size_t)stage * C::kStage;
+          uint8_t* sb = sa + C::kParts * C::kA;
+          mbar_arrive_expect_tx(&full_bar[stage], C::kStage);
+          const int k0 = kb * C::kBK;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              tma_load_3d(sb + q * 8192, &G.map_b, &full_bar[stage], tc.bj * kBN + q * 64, k0, tc.b);
-          } else {
+          for (int part = 0; part < C::kParts; ++part) {
+            const CUtensorMap* ma = part ? &G.map_a_lo : &G.map_a;
+            const CUtensorMap* mb = part ? &G.map_b_lo : &G.map_b;
+            tma_load_3d(sa + part * C::kA, ma, &full_bar[stage], k0, tc.bi * kBM, tc.b);
+            uint8_t* sbp = sb + part * C::kB;
+            if (mn_b) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tma_load_3d(sb + h * 16384, &G.map_b, &full_bar[stage], k0, tc.bj * kBN + h * 128, tc.b);
+              for (int q = 0; q < C::kChunks; ++q)
+                tma_load_3d(sbp + q * C::kChunkBytes, mb, &full_bar[stage], tc.bj * kBN + q * C::kBK, k0, tc.b);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d(sbp + h * (C::kB / 2), mb, &full_bar[stage], k0, tc.bj * kBN + h * (kBN / 2), tc.b);
+            }
           }
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
       }
       if (*abort_p) {
         // let loads already issued land before the CTA exits (bounded)
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s)
           (void)mbar_wait(&full_bar[s], phase ^ (s < stage ? 0u : 1u), nullptr, nullptr, 100000000ull);
-        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      const uint32_t idesc = make_idesc(1u, kBM, kBN, mode == kUpdate ? 1u : 0u);
+      const uint32_t idesc = make_idesc(C::kFormat, kBM, kBN, mn_b ? 1u : 0u);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -181,7 +318,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
       for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile(a, t);
         const GemmGroup& G = a.g[tc.g];
-        const int kblocks = (G.K + kBK - 1) / kBK;
+        const int kblocks = (G.K + C::kBK - 1) / C::kBK;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_p, status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
@@ -189,17 +326,29 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_p, status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
-          const uint32_t sb = sa + kABytes;
+          const uint32_t sa = smem_u32(smem + (size_t)stage * C::kStage);
+          const uint32_t sb = sa + C::kParts * C::kA;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
+          for (int kk = 0; kk < C::kBK / C::kInstK; ++kk) {
             const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = (mode == kUpdate) ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
-                                                  : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            const uint64_t bd = mn_b
+                                    ? smem_desc_sw128(sb + kk * C::kInstK * 128, C::kChunkBytes, 1024)
+                                    : smem_desc_sw128(sb + kk * 32, 16, 1024);
+            const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
+            if (kTF32) {
+              const uint64_t ad_lo = smem_desc_sw128(sa + C::kA + kk * 32, 16, 1024);
+              const uint64_t bd_lo = mn_b
+                                         ? smem_desc_sw128(sb + C::kB + kk * C::kInstK * 128, C::kChunkBytes, 1024)
+                                         : smem_desc_sw128(sb + C::kB + kk * 32, 16, 1024);
+              mma_tf32(d_tmem, ad_lo, bd, idesc, accumulate);
+              mma_tf32(d_tmem, ad, bd_lo, idesc, 1u);
+              mma_tf32(d_tmem, ad, bd, idesc, 1u);
+            } else {
+              mma_bf16(d_tmem, ad, bd, idesc, accumulate);
+            }
           }
           mma_commit(&empty_bar[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit(&tfull_bar[acc]);
@@ -231,8 +380,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
       }
       const bool sym = (mode != kUpdate);
       const int64_t r = (int64_t)tc.bi * kBM + row_in_tile;
-      __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(G.c_hi) + (int64_t)tc.b * G.c_mstride;
-      const __nv_bfloat16* D = reinterpret_cast<const __nv_bfloat16*>(G.d_hi) + (int64_t)tc.b * G.c_mstride;
+      const int64_t mb = (int64_t)tc.b * G.c_mstride;
       const int64_t ld = G.c_ld;
 #pragma unroll 1
       for (int cc = 0; cc < kBN / 32; ++cc) {
@@ -240,48 +388,29 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
         const int64_t c0 = (int64_t)tc.bj * kBN + cc * 32;
         if (r >= G.M || c0 >= G.N) continue;
-        const bool cols_full = (c0 + 32 <= G.N);
+        const int64_t valid = G.N - c0;  // columns of this chunk inside the matrix
         if (mode != kGram) {
-          const __nv_bfloat16* drow = D + r * ld + c0;
-          if (cols_full) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint4 raw = *reinterpret_cast<const uint4*>(drow + 8 * q);
-              const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w4[h]);
-                v[8 * q + 2 * h] = alpha * v[8 * q + 2 * h] + beta * __low2float(p);
-                v[8 * q + 2 * h + 1] = alpha * v[8 * q + 2 * h + 1] + beta * __high2float(p);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              v[j] = alpha * v[j] + (c0 + j < G.N ? beta * __bfloat162float(drow[j]) : 0.f);
-          }
+          Epi<kTF32>::add_d(v, G, mb + r * ld + c0, valid >= 32, valid, alpha, beta);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= alpha;
         }
         // direct store of row r (upper part only in the symmetric modes)
-        __nv_bfloat16* crow = C + r * ld + c0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int64_t cq = c0 + 8 * q;
-          if (cq + 8 <= G.N && (!sym || cq >= r)) {
-            uint4 raw;
-            raw.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-            raw.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-            raw.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-            raw.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-            *reinterpret_cast<uint4*>(crow + 8 * q) = raw;
-          } else {
+          unsigned mask = 0;
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
-              const int64_t c = cq + h;
-              if (c < G.N && (!sym || c >= r)) crow[8 * q + h] = __float2bfloat16_rn(v[8 * q + h]);
-            }
+          for (int h = 0; h < 8; ++h)
+            if (cq + h < G.N && (!sym || cq + h >= r)) mask |= 1u << h;
+          Epi<kTF32>::store8(G, mb + r * ld + cq, v + 8 * q, mask == 0xFFu, mask);
+        }
+        if constexpr (kTF32) {
+          if (mode == kUpdate) {  // X'^T[c][r] for the next UPDATE's K-major B operand
+            const int64_t mbt = (int64_t)tc.b * G.ct_mstride;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j < G.N) Epi<true>::store1t(G, mbt + (c0 + j) * G.ct_ld + r, v[j]);
           }
         }
         // mirror of the strictly upper part: C[c][r] = C[r][c]
@@ -289,7 +418,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int64_t c = c0 + j;
-            if (c > r && c < G.N) C[c * ld + r] = __float2bfloat16_rn(v[j]);
+            if (c > r && c < G.N) Epi<kTF32>::store1(G, mb + c * ld + r, v[j]);
           }
         }
       }
@@ -309,26 +438,27 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_bf16_kernel(const __grid
   }
 }
 
-}  // namespace
-
-size_t gemm_smem_bytes(bool tf32) {
-  (void)tf32;
-  return kSmemBytes;
-}
-
-cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, cudaStream_t s) {
-  if (tf32) return cudaErrorNotSupported;
-  if (a.total_tiles <= 0) return cudaSuccess;
+template <bool kTF32>
+cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ns_gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cfg<kTF32>::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int grid = a.total_tiles < num_sms ? a.total_tiles : num_sms;
-  ns_gemm_bf16_kernel<<<grid, kThreadsG, kSmemBytes, s>>>(a);
+  ns_gemm_kernel<kTF32><<<grid, kThreadsG, Cfg<kTF32>::kSmem, s>>>(a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(bool tf32) { return tf32 ? Cfg<true>::kSmem : Cfg<false>::kSmem; }
+
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, cudaStream_t s) {
+  if (a.total_tiles <= 0) return cudaSuccess;
+  return tf32 ? launch_impl<true>(a, num_sms, s) : launch_impl<false>(a, num_sms, s);
 }
 
 }  // namespace muon

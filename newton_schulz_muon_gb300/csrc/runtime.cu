@@ -81,11 +81,15 @@ struct BGroup {
   int64_t mat_base;      // bucket-local index of the group's first matrix
   int64_t ld_n, ld_m;    // leading dimensions in the workspace
   std::vector<Run> runs;
-  // byte offsets inside the NS region (hi parts; lo parts for 3xTF32)
+  // byte offsets inside the NS region (hi parts; lo parts and X^T for 3xTF32)
   size_t off_x[2], off_a, off_b;
   size_t off_x_lo[2], off_a_lo, off_b_lo;
-  // tensor maps encoded at bind time
+  size_t off_xt[2], off_xt_lo[2];
+  int64_t ld_t;          // leading dimension of X^T (n x m)
+  // tensor maps encoded at bind time (lo parts: 3xTF32 only)
   CUtensorMap kx[2], mx[2], ka, kb;
+  CUtensorMap kx_lo[2], mx_lo[2], ka_lo, kb_lo;
+  CUtensorMap kxt[2], kxt_lo[2];
 };
 
 struct Bucket {
@@ -184,12 +188,17 @@ void layout_bucket(Bucket& b, const muon_config& cfg) {
     for (int i = 0; i < 2; ++i) { g.off_x[i] = off; off = align_up(off + xb, kAlign); }
     g.off_a = off; off = align_up(off + ab, kAlign);
     g.off_b = off; off = align_up(off + ab, kAlign);
+    g.ld_t = round_up(g.m, 8);
     if (tf32) {
+      const size_t tb = (size_t)g.count * g.n * g.ld_t * es;
       for (int i = 0; i < 2; ++i) { g.off_x_lo[i] = off; off = align_up(off + xb, kAlign); }
       g.off_a_lo = off; off = align_up(off + ab, kAlign);
       g.off_b_lo = off; off = align_up(off + ab, kAlign);
+      for (int i = 0; i < 2; ++i) { g.off_xt[i] = off; off = align_up(off + tb, kAlign); }
+      for (int i = 0; i < 2; ++i) { g.off_xt_lo[i] = off; off = align_up(off + tb, kAlign); }
     } else {
       g.off_x_lo[0] = g.off_x_lo[1] = g.off_a_lo = g.off_b_lo = 0;
+      g.off_xt[0] = g.off_xt[1] = g.off_xt_lo[0] = g.off_xt_lo[1] = 0;
     }
   }
   b.ns_bytes = off;
@@ -334,6 +343,13 @@ void make_prep_args(const muon_plan_t* p, const Bucket& b, F ptr, float mu, int 
       s.x_ld = g.ld_n;
       s.x_mstride = g.m * g.ld_n;
       s.block0 = tile;
+      if (tf32) {
+        const int64_t toff = (mat - g.mat_base) * g.n * g.ld_t;
+        s.xt_hi = reinterpret_cast<float*>(p->ws + p->off_ns + g.off_xt[0]) + toff;
+        s.xt_lo = reinterpret_cast<float*>(p->ws + p->off_ns + g.off_xt_lo[0]) + toff;
+        s.xt_ld = g.ld_t;
+        s.xt_mstride = g.n * g.ld_t;
+      }
       s.count = (int32_t)r.count;
       s.transposed = t.transposed ? 1 : 0;
       s.tiles_c = (int32_t)cdiv(t.cols, kPrepTile);
@@ -434,19 +450,32 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
         uint8_t* ns = p->ws + p->off_ns;
         G.count = (int32_t)g.count;
         G.mat_base = (int32_t)g.mat_base;
+        auto lo = [&](size_t off) { return tf32 ? reinterpret_cast<float*>(ns + off) : nullptr; };
         if (mode == kGram) {
           G.map_a = g.kx[cur]; G.map_b = g.kx[cur];
-          G.c_hi = ns + g.off_a; G.d_hi = nullptr;
+          if (tf32) { G.map_a_lo = g.kx_lo[cur]; G.map_b_lo = g.kx_lo[cur]; }
+          G.c_hi = ns + g.off_a; G.c_lo = lo(g.off_a_lo);
+          G.d_hi = nullptr; G.d_lo = nullptr;
           G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
           G.M = (int32_t)g.m; G.N = (int32_t)g.m; G.K = (int32_t)g.n;
         } else if (mode == kPoly) {
           G.map_a = g.ka; G.map_b = g.ka;
-          G.c_hi = ns + g.off_b; G.d_hi = ns + g.off_a;
+          if (tf32) { G.map_a_lo = g.ka_lo; G.map_b_lo = g.ka_lo; }
+          G.c_hi = ns + g.off_b; G.c_lo = lo(g.off_b_lo);
+          G.d_hi = ns + g.off_a; G.d_lo = lo(g.off_a_lo);
           G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
           G.M = (int32_t)g.m; G.N = (int32_t)g.m; G.K = (int32_t)g.m;
         } else {
           G.map_a = g.kb; G.map_b = g.mx[cur];
-          G.c_hi = ns + g.off_x[nxt]; G.d_hi = ns + g.off_x[cur];
+          if (tf32) {
+            // 3xTF32 reads the rows of X^T (K-major) and writes X'^T as well
+            G.map_a_lo = g.kb_lo;
+            G.map_b = g.kxt[cur]; G.map_b_lo = g.kxt_lo[cur];
+            G.ct_hi = ns + g.off_xt[nxt]; G.ct_lo = lo(g.off_xt_lo[nxt]);
+            G.ct_ld = g.ld_t; G.ct_mstride = g.n * g.ld_t;
+          }
+          G.c_hi = ns + g.off_x[nxt]; G.c_lo = lo(g.off_x_lo[nxt]);
+          G.d_hi = ns + g.off_x[cur]; G.d_lo = lo(g.off_x_lo[cur]);
           G.c_ld = g.ld_n; G.c_mstride = g.m * g.ld_n;
           G.M = (int32_t)g.m; G.N = (int32_t)g.n; G.K = (int32_t)g.m;
         }
@@ -621,6 +650,18 @@ muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes
       }
       ok &= encode_map(&g.ka, ns + g.off_a, es, g.m, g.m, g.count, g.ld_m, kbox, 128);
       ok &= encode_map(&g.kb, ns + g.off_b, es, g.m, g.m, g.count, g.ld_m, kbox, 128);
+      if (tf32) {
+        for (int i = 0; i < 2; ++i) {
+          ok &= encode_map(&g.kx_lo[i], ns + g.off_x_lo[i], es, g.n, g.m, g.count, g.ld_n, kbox, 128);
+          ok &= encode_map(&g.mx_lo[i], ns + g.off_x_lo[i], es, g.n, g.m, g.count, g.ld_n, kbox, kbox);
+        }
+        ok &= encode_map(&g.ka_lo, ns + g.off_a_lo, es, g.m, g.m, g.count, g.ld_m, kbox, 128);
+        ok &= encode_map(&g.kb_lo, ns + g.off_b_lo, es, g.m, g.m, g.count, g.ld_m, kbox, 128);
+        for (int i = 0; i < 2; ++i) {  // X^T: n rows of m
+          ok &= encode_map(&g.kxt[i], ns + g.off_xt[i], es, g.m, g.n, g.count, g.ld_t, kbox, 128);
+          ok &= encode_map(&g.kxt_lo[i], ns + g.off_xt_lo[i], es, g.m, g.n, g.count, g.ld_t, kbox, 128);
+        }
+      }
       if (!ok) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled rejected a workspace tensor map");
     }
   }
@@ -659,7 +700,6 @@ muon_status muon_step(muon_plan_t* p, void* const* params, const void* const* gr
     return fail(MUON_ERR_INVALID, "n_mats %lld != %zu tensors in the plan", (long long)n_mats, p->tensors.size());
   if (ns_steps < 0 || ns_steps > 16) return fail(MUON_ERR_INVALID, "ns_steps must be in [0, 16]");
   if (!std::isfinite(lr) || !std::isfinite(mu) || !std::isfinite(wd)) return fail(MUON_ERR_INVALID, "lr, mu, wd must be finite");
-  if (p->cfg.ns_precision == MUON_NS_TF32X3) return fail(MUON_ERR_UNSUPPORTED, "3xTF32 Newton-Schulz is not built yet");
   for (int i = 0; i < n_mats; ++i) {
     muon_status s;
     if ((s = check_device_ptr(params[i], "params", i)) != MUON_OK) return s;
@@ -715,7 +755,6 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
   if (n_mats != (int64_t)p->tensors.size())
     return fail(MUON_ERR_INVALID, "n_mats %lld != %zu tensors in the plan", (long long)n_mats, p->tensors.size());
   if (ns_steps < 0 || ns_steps > 16) return fail(MUON_ERR_INVALID, "ns_steps must be in [0, 16]");
-  if (p->cfg.ns_precision == MUON_NS_TF32X3) return fail(MUON_ERR_UNSUPPORTED, "3xTF32 Newton-Schulz is not built yet");
   if (timeout_ms <= 0) return fail(MUON_ERR_INVALID, "timeout_ms must be > 0");
   for (int i = 0; i < n_mats; ++i) {
     muon_status s;

@@ -172,3 +172,115 @@ def test_argument_validation_on_device(m):
     with pytest.raises(m.MuonError) as e:
         m.muon_plan_bind_workspace(m.muon_plan(wl.plan_shapes()), small)
     assert e.value.status == m.MUON_ERR_NO_WORKSPACE
+
+
+# --- fp32 (3xTF32) Newton-Schulz mode: per-matrix tolerance 1e-4 --------------
+
+@pytest.mark.parametrize("shapes", [[(256, 512)], [(300, 200), (100, 700)], [(128, 384, 3), (640, 384)],
+                                    [(1, 64), (130, 130)]])
+def test_tf32x3_mode(m, shapes):
+    from gpu_util import TOL_TF32X3
+    wl = Workload(shapes, m_sigma=0.02, g_sigma=1e-3)
+    cfg = m.muon_config_default(ns_precision=m.MUON_NS_TF32X3)
+    ulp, rel = _run(m, wl, cfg=cfg, tol=TOL_TF32X3, steps=2)
+    assert rel <= TOL_TF32X3
+
+
+@pytest.mark.parametrize("coeffs", [(1.0, 0.0, 0.0), (0.0, 1.0, 0.0), (0.0, 0.0, 1.0)])
+def test_tf32x3_one_iteration_each_gemm(m, coeffs):
+    from gpu_util import TOL_TF32X3
+    wl = Workload([(192, 320), (320, 192)], w_sigma=0.0, g_sigma=1.0, g_dtype=synth.F32)
+    cfg = m.muon_config_default(ns_precision=m.MUON_NS_TF32X3)
+    _run(m, wl, cfg=cfg, ns_steps=1, coeffs=coeffs, mu=0.0, nesterov=False, tol=TOL_TF32X3)
+
+
+# --- offload: pinned host gradients and momentum --------------------------------
+
+def _pinned(arr, dtype_code):
+    import torch
+    if dtype_code == synth.BF16:
+        t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32))
+    return t.pin_memory()
+
+
+def _offload(m, wl, cap, inflight, ns_steps=5, mu=0.95):
+    import torch
+    cfg = m.muon_config_default(offload=1, max_inflight=inflight, timing=1)
+    cfg.grad_dtype = wl.g_dtype
+    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=cfg)
+    m.allocate_workspace(plan)
+    hG = [_pinned(g, wl.g_dtype) for g in wl.G]
+    hM = [_pinned(x, synth.F32) for x in wl.M]
+    hU = [torch.empty(x.shape, dtype=torch.float32).pin_memory() for x in wl.M]
+    m.muon_offload_step(plan, hG, hM, hU, mu, True, ns_steps, timeout_ms=120_000)
+    st = m.muon_get_stats(plan)
+    return [x.numpy().copy() for x in hM], [u.numpy().copy() for u in hU], st, plan
+
+
+def test_offload_matches_oracle_and_is_order_independent(m):
+    shapes = [(256, 512), (300, 200, 2), (64, 640), (512, 128, 3)]
+    wl = Workload(shapes, m_sigma=0.02, g_sigma=1e-3)
+    M1, U1, st, plan = _offload(m, wl, cap=400_000, inflight=1)
+    assert m.muon_get_plan_info(plan).n_buckets >= 3
+    assert st.h2d_bytes > 0 and st.d2h_bytes > 0
+    mu32, omu = oracle_constants(0.95, "ema")
+    for i, (r, c, k) in enumerate(wl.shapes):
+        for j in range(k):
+            G = widen(wl.G[i][j], wl.g_dtype)
+            Mo = oracle.momentum_update(wl.M[i][j], G, mu32, one_minus_mu=omu)
+            assert int(ulp_distance(M1[i][j], Mo).max()) <= 1
+            V = oracle.nesterov_blend(Mo, G, mu32, True, one_minus_mu=omu)
+            Uo = oracle.offload_update(oracle.newton_schulz(V, coeffs=tuple(f32(v) for v in oracle.DEFAULT_COEFFS),
+                                                            eps=f32(1e-7)), r, c)
+            assert rel_fro(U1[i][j], Uo) <= TOL_BF16, (i, j)
+    # two buckets in writeback while one computes gives the same bytes
+    M2, U2, _, _ = _offload(m, wl, cap=400_000, inflight=2)
+    for a, b in zip(M1 + U1, M2 + U2):
+        assert np.array_equal(a, b)
+
+
+def test_offload_rejects_pageable_host_memory(m):
+    import torch
+    wl = Workload([(64, 128)])
+    cfg = m.muon_config_default(offload=1)
+    plan = m.muon_plan(wl.plan_shapes(), config=cfg)
+    m.allocate_workspace(plan)
+    g = torch.zeros((64, 128), dtype=torch.bfloat16)          # pageable
+    mm = torch.zeros((64, 128), dtype=torch.float32).pin_memory()
+    u = torch.zeros((64, 128), dtype=torch.float32).pin_memory()
+    with pytest.raises(m.MuonError) as e:
+        m.muon_offload_step(plan, [g], [mm], [u], 0.95, True, 5)
+    assert e.value.status == m.MUON_ERR_NOT_PINNED
+    plan2 = m.muon_plan(wl.plan_shapes())                      # no staging slots
+    m.allocate_workspace(plan2)
+    with pytest.raises(m.MuonError) as e:
+        m.muon_offload_step(plan2, [g.pin_memory()], [mm], [u], 0.95, True, 5)
+    assert e.value.status == m.MUON_ERR_NO_WORKSPACE
+
+
+def test_resume_from_copied_state_is_bitwise_identical(m):
+    import torch
+    shapes = [(256, 384, 2), (384, 256)]
+    run = Workload(shapes, m_sigma=0.0, g_sigma=1e-3)
+    plan = m.muon_plan(run.plan_shapes())
+    m.allocate_workspace(plan)
+    for step in range(4):
+        run.new_grads(step)
+        m.muon_step(plan, run.dW, run.dG, run.dM, 0.02, 0.95, True, 0.01, 5)
+        if step == 1:   # checkpoint: copy the caller-owned state out
+            ckpt = [t.cpu().clone() for t in run.dW + run.dM]
+    torch.cuda.synchronize()
+    res = Workload(shapes, m_sigma=0.0, g_sigma=1e-3)
+    n = len(shapes)
+    res.dW = [t.cuda() for t in ckpt[:n]]
+    res.dM = [t.cuda() for t in ckpt[n:]]
+    plan2 = m.muon_plan(res.plan_shapes())                      # fresh plan and workspace
+    m.allocate_workspace(plan2)
+    for step in (2, 3):
+        res.new_grads(step)
+        m.muon_step(plan2, res.dW, res.dG, res.dM, 0.02, 0.95, True, 0.01, 5)
+    torch.cuda.synchronize()
+    for a, b in zip(run.dW + run.dM, res.dW + res.dM):
+        assert torch.equal(a, b)
