@@ -123,15 +123,90 @@ def check_step(wl: Workload, W_prev, M_prev, W_new, M_new, *, lr, mu, nesterov, 
                                                 c32, f32(eps), form, one_minus_mu=omu)
             ulp = int(ulp_distance(M_new[i][j], Mo).max())
             assert ulp <= 1, f"tensor {i} matrix {j}: momentum differs by {ulp} ulp"
-            dW_gpu = widen(W_new[i][j], wl.w_dtype) - Wp
-            dW_or = Wo - Wp
-            rel = rel_fro(dW_gpu, dW_or)
-            allowed = tol
             if wl.w_dtype == synth.BF16:
-                # the stored weight is rounded to bf16: half an ulp of bf16 per element
-                ulp16 = np.abs(Wo) * 2.0 ** -8
-                allowed = tol + float(np.linalg.norm(0.5 * ulp16) / max(np.linalg.norm(dW_or), 1e-30))
-            assert rel <= allowed, f"tensor {i} matrix {j} ({r}x{c}): rel update error {rel:.3e} > {allowed:.1e}"
+                bf16_weight_check(W_new[i][j], Wo, Wp, tol)
+                rel = 0.0
+            else:
+                rel = rel_fro(widen(W_new[i][j], wl.w_dtype) - Wp, Wo - Wp)
+                assert rel <= tol, f"tensor {i} matrix {j} ({r}x{c}): rel update error {rel:.3e} > {tol:.1e}"
             worst_ulp = max(worst_ulp, ulp)
             worst_rel = max(worst_rel, rel)
     return worst_ulp, worst_rel
+
+
+def bf16_weight_check(W_new_bits, Wo, Wp, tol):
+    """bf16 weights: W_new = bf16(W_or + d) with ||d|| <= tol ||dW_or||, so
+    ||W_new - W_or|| <= tol ||dW_or|| + || |W_or| 2^-8 || (a bf16 half-ulp is at most
+    2^-8 of the value).  Returns the measured left side over ||dW_or||."""
+    err = np.linalg.norm(synth.as_f64(W_new_bits, synth.BF16) - Wo)
+    den = max(np.linalg.norm(Wo - Wp), 1e-30)
+    bound = tol * den + np.linalg.norm(np.abs(Wo) * 2.0 ** -8)
+    assert err <= bound, f"bf16 weights: error {err:.3e} above the bound {bound:.3e}"
+    return float(err / den)
+
+
+def run_steps(m, wl, *, lr=0.02, mu=0.95, nesterov=True, wd=0.0, ns_steps=5, cap=512 << 20, cfg=None,
+              steps=1, form="ema", coeffs=oracle.DEFAULT_COEFFS, sample=None, tol=TOL_BF16):
+    """Run `steps` GPU Muon steps on a Workload, checking each against the oracle."""
+    import torch
+    cfg = cfg or m.muon_config_default()
+    cfg.grad_dtype = wl.g_dtype
+    cfg.param_dtype = wl.w_dtype
+    cfg.momentum_form = m.MUON_MOMENTUM_SGD if form == "sgd" else m.MUON_MOMENTUM_EMA
+    cfg.ns_a, cfg.ns_b, cfg.ns_c = coeffs
+    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=cfg)
+    m.allocate_workspace(plan)
+    worst = (0, 0.0)
+    for step in range(steps):
+        if step > 0:
+            wl.new_grads(step)
+        W_prev = [to_numpy(t, wl.w_dtype) for t in wl.dW]
+        M_prev = [to_numpy(t, synth.F32) for t in wl.dM]
+        m.muon_step(plan, wl.dW, wl.dG, wl.dM, lr, mu, nesterov, wd, ns_steps)
+        st, nf = m.muon_sync(plan)
+        assert st == m.MUON_OK and nf == 0
+        torch.cuda.synchronize()
+        W_new = [to_numpy(t, wl.w_dtype) for t in wl.dW]
+        M_new = [to_numpy(t, synth.F32) for t in wl.dM]
+        u, r = check_step(wl, W_prev, M_prev, W_new, M_new, lr=lr, mu=mu, nesterov=nesterov, wd=wd,
+                          ns_steps=ns_steps, coeffs=coeffs, form=form, sample=sample, tol=tol)
+        worst = (max(worst[0], u), max(worst[1], r))
+    return worst
+
+
+def device_tensor(shape, dtype_code, seed, stream, step, sigma):
+    """A seeded tensor filled on the device (bit-identical to synth.tensor)."""
+    import torch
+    dt = torch.bfloat16 if dtype_code == synth.BF16 else torch.float32
+    t = torch.empty(shape, dtype=dt, device="cuda")
+    if sigma > 0:
+        synth.fill_normal_cuda(t, seed, stream, step, sigma)
+    else:
+        t.zero_()
+    return t
+
+
+def host_matrix(shape_rc, index, dtype_code, seed, stream, step, sigma):
+    """Matrix `index` of a [count, rows, cols] seeded tensor, generated on the CPU."""
+    r, c = shape_rc
+    if sigma <= 0:
+        return np.zeros((r, c), np.uint16 if dtype_code == synth.BF16 else np.float32)
+    return synth.tensor(seed, stream, step, (r, c), sigma, dtype_code, start=index * r * c)
+
+
+def check_matrix(W_prev, M_prev, G, W_new, M_new, *, w_dtype, g_dtype, lr, mu, nesterov=True, wd=0.0,
+                 ns_steps=5, form="ema", tol=TOL_BF16):
+    """Teacher-forced oracle comparison of one logical matrix; returns (ulp, rel)."""
+    mu32, omu = oracle_constants(mu, form)
+    c32 = tuple(f32(v) for v in oracle.DEFAULT_COEFFS)
+    Wp = widen(W_prev, w_dtype)
+    Wo, Mo, _ = oracle.muon_matrix_step(Wp, M_prev, widen(G, g_dtype), f32(lr), mu32, nesterov, f32(wd),
+                                        ns_steps, c32, f32(1e-7), form, one_minus_mu=omu)
+    ulp = int(ulp_distance(M_new, Mo).max())
+    assert ulp <= 1, f"momentum differs by {ulp} ulp"
+    if w_dtype == synth.BF16:
+        bf16_weight_check(W_new, Wo, Wp, tol)
+        return ulp, 0.0
+    rel = rel_fro(widen(W_new, w_dtype) - Wp, Wo - Wp)
+    assert rel <= tol, f"rel update error {rel:.3e} > {tol:.2e}"
+    return ulp, rel

@@ -10,8 +10,8 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import (TOL_BF16, Workload, check_step, f32, nsm, oracle_constants, rel_fro, to_numpy,
-                      torch_from, ulp_distance, widen)
+from gpu_util import (TOL_BF16, Workload, f32, nsm, oracle_constants, rel_fro, run_steps, to_numpy,
+                      ulp_distance, widen)
 
 pytestmark = pytest.mark.gpu
 
@@ -21,32 +21,8 @@ def m():
     return nsm()
 
 
-def _run(m, wl, *, lr=0.02, mu=0.95, nesterov=True, wd=0.0, ns_steps=5, cap=512 << 20, cfg=None,
-         steps=1, form="ema", coeffs=oracle.DEFAULT_COEFFS, sample=None, tol=TOL_BF16):
-    import torch
-    cfg = cfg or m.muon_config_default()
-    cfg.grad_dtype = wl.g_dtype
-    cfg.param_dtype = wl.w_dtype
-    cfg.momentum_form = m.MUON_MOMENTUM_SGD if form == "sgd" else m.MUON_MOMENTUM_EMA
-    cfg.ns_a, cfg.ns_b, cfg.ns_c = coeffs
-    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=cfg)
-    m.allocate_workspace(plan)
-    worst = (0, 0.0)
-    for step in range(steps):
-        if step > 0:
-            wl.new_grads(step)
-        W_prev = [to_numpy(t, wl.w_dtype) for t in wl.dW]
-        M_prev = [to_numpy(t, synth.F32) for t in wl.dM]
-        m.muon_step(plan, wl.dW, wl.dG, wl.dM, lr, mu, nesterov, wd, ns_steps)
-        st, nf = m.muon_sync(plan)
-        assert st == m.MUON_OK and nf == 0
-        torch.cuda.synchronize()
-        W_new = [to_numpy(t, wl.w_dtype) for t in wl.dW]
-        M_new = [to_numpy(t, synth.F32) for t in wl.dM]
-        u, r = check_step(wl, W_prev, M_prev, W_new, M_new, lr=lr, mu=mu, nesterov=nesterov, wd=wd,
-                          ns_steps=ns_steps, coeffs=coeffs, form=form, sample=sample, tol=tol)
-        worst = (max(worst[0], u), max(worst[1], r))
-    return worst
+def _run(m, wl, **kw):
+    return run_steps(m, wl, **kw)
 
 
 def test_synth_device_fill_is_bit_identical(m):
