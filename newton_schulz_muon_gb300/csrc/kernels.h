@@ -108,7 +108,7 @@ struct GemmGroup {
   int64_t ct_ld, ct_mstride;
   int32_t M, N, K;           // output rows, cols, reduction length
   int32_t count;             // matrices
-  int32_t tiles_m, tiles_n;  // tile grid of one matrix
+  int32_t tiles_m, tiles_n;  // row blocks (kBM * cluster rows) and 256-column blocks of one matrix
   int32_t tiles_per_mat;     // tiles computed per matrix (upper triangle for GRAM/POLY)
   int32_t tile0;             // first launch-wide tile index of this group
   int32_t mat_base;          // bucket-local index of matrix 0 (for the scale array)
@@ -134,7 +134,9 @@ constexpr int kBN = 256;
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_norm(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t s);
-cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, cudaStream_t s);
+// cluster: 1, or 2 (pairs of vertically adjacent tiles share the B operand);
+// GemmGroup::tiles_m counts row blocks of kBM * cluster rows.
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, int cluster, cudaStream_t s);
 size_t gemm_smem_bytes(bool tf32);
 
 // Records `msg` as the calling thread's muon_last_error text and returns `s`.

@@ -20,19 +20,30 @@
 // In the first iteration X holds the un-normalised V; the per-matrix factor
 // s = 1/(||V||_F + eps) is applied in the epilogues (GRAM: s^2, UPDATE: s).
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0  lane 0: TMA producer over a shared-memory ring of 128-byte-swizzled
+// Kernel structure (one persistent CTA per SM, 320 threads):
+//   warp 0:         TMA producer (converged warp, lane 0 issues) over a shared-memory ring of 128-byte-swizzled
 //                   stages: bf16 -- 4 stages of A 128 x 64 + B 256 x 64;
 //                   3xTF32 -- 2 stages of A 128 x 32 and B 256 x 32, each as a
 //                   tf32-high and a tf32-low fp32 copy
-//   warp 1  lane 0: tcgen05.mma issuer, M=128 N=256 (K=16 bf16 / K=8 tf32), fp32
+//   warp 1:         tcgen05.mma issuer (converged warp, lane 0 issues), M=128 N=256 (K=16 bf16 / K=8 tf32), fp32
 //                   accumulators in TMEM, two accumulator buffers (512 columns)
 //                   so the epilogue of one tile overlaps the main loop of the
 //                   next.  3xTF32 issues hi*hi + hi*lo + lo*hi per k step.
-//   warps 2-5:      epilogue; warp w reads TMEM lanes 32*(w%4)..+31 with
-//                   tcgen05.ld, applies alpha/beta, converts to bf16 and stores.
+//   warps 2-9:      epilogue; warp w reads TMEM lanes 32*(w%4)..+31 with
+//                   tcgen05.ld (two warps per lane quadrant, 128 columns each),
+//                   applies alpha/beta, converts and stores.
 // Tiles of all same-shape groups of a micro-bucket (and of all its matrices) are
-// numbered in one space and dealt round-robin to the CTAs.
+// numbered in one space and dealt round-robin to the CTAs (groups ordered by
+// reduction length, longest first).
+//
+// kCL = 2 (the default for m > 128): a cluster of two CTAs on two SMs computes a
+// 256 x 256 tile with one tcgen05.mma.cta_group::2 (M=256, N=256) issued by the
+// even CTA.  Each CTA holds its own 128 rows of A and one 128-wide half of B, so
+// each SM streams half as many B bytes through its shared memory as a single-SM
+// 128 x 256 tile (whose operand reads plus TMA fills otherwise saturate shared
+// memory bandwidth).  Both CTAs' TMA loads complete on the even CTA's barrier;
+// its commits release stages and accumulators in both CTAs; each CTA drains the
+// 128 accumulator rows in its own Tensor Memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -44,24 +55,29 @@
 namespace muon {
 namespace {
 
-constexpr int kThreadsG = 192;
+constexpr int kThreadsG = 320;  // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t kTmemCols = 512;
 
-// Per-precision constants.  A "part" is one copy of an operand tile: bf16 has one,
-// 3xTF32 has a tf32-high and a tf32-low fp32 copy.  Rows are 128 bytes (one
-// swizzle atom wide), so a part of A is 16 KB and a part of B 32 KB in both modes.
-template <bool kTF32>
+// Per-precision, per-cluster-size constants.  A "part" is one copy of an operand
+// tile: bf16 has one, 3xTF32 a tf32-high and a tf32-low fp32 copy.  Rows are 128
+// bytes (one swizzle atom wide).  Each CTA holds 128 rows of A and kBN / kCL rows
+// (K-major) or columns (MN-major) of B per part.
+template <bool kTF32, int kCL>
 struct Cfg {
-  static constexpr int kBK = kTF32 ? 32 : 64;           // k elements per 128-byte row
-  static constexpr int kStages = kTF32 ? 2 : 4;
+  static constexpr int kBK = kTF32 ? 32 : 64;            // k elements per 128-byte row
   static constexpr int kParts = kTF32 ? 2 : 1;
-  static constexpr uint32_t kA = kBM * 128;              // 16 KB
-  static constexpr uint32_t kB = kBN * 128;              // 32 KB
+  static constexpr uint32_t kA = kBM * 128;               // 16 KB
+  static constexpr int kBRows = kBN / kCL;                // B rows (or columns) held by one CTA
+  static constexpr uint32_t kB = kBRows * 128;            // 32 KB or 16 KB
   static constexpr uint32_t kStage = kParts * (kA + kB);
-  static constexpr int kInstK = kTF32 ? 8 : 16;          // k per MMA instruction
-  static constexpr int kChunks = kBN / kBK;              // MN-major: 128-byte column chunks per tile
-  static constexpr uint32_t kChunkBytes = kBK * 128;     // one chunk: kBK k-rows of 128 B
-  static constexpr uint32_t kFormat = kTF32 ? 2u : 1u;   // tf32 / bf16 in the instruction descriptor
+  // as many stages as fit in the 227 KB of dynamic shared memory a CTA may use
+  // (1 KB kept for the 1024-byte alignment of the ring, 1 KB for static data)
+  static constexpr int kStages = (int)((232448u - 2048u) / kStage);
+  static constexpr uint32_t kTx = kCL * kStage;           // bytes landing per stage on the leader's barrier
+  static constexpr int kInstK = kTF32 ? 8 : 16;           // k per MMA instruction
+  static constexpr int kChunks = kBRows / kBK;            // MN-major 128-byte column chunks per CTA
+  static constexpr uint32_t kChunkBytes = kBK * 128;      // one chunk: kBK k-rows of 128 B
+  static constexpr uint32_t kFormat = kTF32 ? 2u : 1u;    // tf32 / bf16 in the instruction descriptor
   static constexpr size_t kSmem = (size_t)kStages * kStage + 1024;
 };
 
@@ -69,7 +85,11 @@ struct TileCoord {
   int g, b, bi, bj;
 };
 
-__device__ __forceinline__ TileCoord decode_tile(const GemmArgs& a, int t) {
+// Tile t of the launch -> group, matrix, row block and column block.  Row blocks
+// are kBM * kCL rows high (one per cluster); the CTA of rank `rank` takes 128-row
+// tile bi = row_block * kCL + rank.
+template <int kCL>
+__device__ __forceinline__ TileCoord decode_tile(const GemmArgs& a, int t, int rank) {
   int g = 0;
   for (int i = 1; i < a.n_groups; ++i)
     if (a.g[i].tile0 <= t) g = i;
@@ -79,23 +99,24 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& a, int t) {
   tc.g = g;
   tc.b = local / G.tiles_per_mat;
   int tt = local % G.tiles_per_mat;
+  int pi = 0;
   if (a.mode == kUpdate) {
-    tc.bi = tt / G.tiles_n;
+    pi = tt / G.tiles_n;
     tc.bj = tt % G.tiles_n;
   } else {
-    // upper-triangle tiles, column block by column block
-    tc.bi = 0;
+    // upper-triangle row blocks, column block by column block
     tc.bj = 0;
     for (int bj = 0; bj < G.tiles_n; ++bj) {
-      const int cnt = min(G.tiles_m, (bj * kBN + kBN - 1) / kBM + 1);
+      const int cnt = min(G.tiles_m, (bj * kBN + kBN - 1) / (kBM * kCL) + 1);
       if (tt < cnt) {
-        tc.bi = tt;
+        pi = tt;
         tc.bj = bj;
         break;
       }
       tt -= cnt;
     }
   }
+  tc.bi = pi * kCL + rank;
   return tc;
 }
 
@@ -212,9 +233,10 @@ struct Epi<true> {  // 3xTF32: fp32 tf32-high + fp32 low parts
   }
 };
 
-template <bool kTF32>
+template <bool kTF32, int kCL>
 __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs a) {
-  using C = Cfg<kTF32>;
+  using C = Cfg<kTF32, kCL>;
+  static_assert(kCL == 1 || kCL == 2, "one CTA, or a pair of CTAs on two SMs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -228,6 +250,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = kCL > 1 ? (int)cluster_ctarank() : 0;
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x / kCL;
+  const int n_clusters = gridDim.x / kCL;
+  constexpr uint16_t kPair = (1u << kCL) - 1u;
   unsigned* status = &a.status->flags;
   volatile int* abort_p = &abort_flag;
 
@@ -238,7 +265,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull_bar[i], 1);
-      mbar_init(&tempty_bar[i], 128);
+      // single CTA: every epilogue thread arrives; pair: one lane per epilogue warp of both CTAs
+      mbar_init(&tempty_bar[i], kCL == 1 ? 256 : 8 * kCL);
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -255,119 +283,158 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     }
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<kCL>(&tmem_slot, kTmemCols);
+    tmem_relinquish<kCL>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kCL > 1) cluster_sync();  // barriers of both CTAs exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = tmem_slot;
   const int mode = a.mode;
   const bool mn_b = (mode == kUpdate) && !kTF32;  // B operand read MN-major
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
-        const TileCoord tc = decode_tile(a, t);
-        const GemmGroup& G = a.g[tc.g];
-        const int kblocks = (G.K + C::kBK - 1) / C::kBK;
-        bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_p, status)) { ok = false; break; }
+    // ---------------- TMA producer (both CTAs) ----------------
+    // The whole warp walks the schedule and waits (converged); lane 0 issues.
+    // Issuing from a lone lane of a diverged warp is several times slower.
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = cluster_id; t < a.total_tiles; t += n_clusters) {
+      const TileCoord tc = decode_tile<kCL>(a, t, rank);
+      const GemmGroup& G = a.g[tc.g];
+      const int kblocks = (G.K + C::kBK - 1) / C::kBK;
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const bool got = mbar_wait(&empty_bar[stage], phase ^ 1u, abort_p, status);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        if (lane == 0) {
           uint8_t* sa = smem + (size_t)stage * C::kStage;
           uint8_t* sb = sa + C::kParts * C::kA;
-          mbar_arrive_expect_tx(&full_bar[stage], C::kStage);
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], C::kTx);
+          const uint32_t bar = kCL > 1 ? mapa_shared(&full_bar[stage], 0) : smem_u32(&full_bar[stage]);
           const int k0 = kb * C::kBK;
 #pragma unroll
           for (int part = 0; part < C::kParts; ++part) {
             const CUtensorMap* ma = part ? &G.map_a_lo : &G.map_a;
             const CUtensorMap* mb = part ? &G.map_b_lo : &G.map_b;
-            tma_load_3d(sa + part * C::kA, ma, &full_bar[stage], k0, tc.bi * kBM, tc.b);
             uint8_t* sbp = sb + part * C::kB;
-            if (mn_b) {
+            if constexpr (kCL == 1) {
+              tma_load_3d(sa + part * C::kA, ma, &full_bar[stage], k0, tc.bi * kBM, tc.b);
+              if (mn_b) {
 #pragma unroll
-              for (int q = 0; q < C::kChunks; ++q)
-                tma_load_3d(sbp + q * C::kChunkBytes, mb, &full_bar[stage], tc.bj * kBN + q * C::kBK, k0, tc.b);
+                for (int q = 0; q < C::kChunks; ++q)
+                  tma_load_3d(sbp + q * C::kChunkBytes, mb, &full_bar[stage], tc.bj * kBN + q * C::kBK, k0, tc.b);
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                  tma_load_3d(sbp + h * (C::kB / 2), mb, &full_bar[stage], k0, tc.bj * kBN + h * 128, tc.b);
+              }
             } else {
+              // own 128 rows of A and own half of B, completing on the even CTA's barrier
+              tma_load_3d_pair(sa + part * C::kA, ma, bar, k0, tc.bi * kBM, tc.b);
+              if (mn_b) {
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
-                tma_load_3d(sbp + h * (C::kB / 2), mb, &full_bar[stage], k0, tc.bj * kBN + h * (kBN / 2), tc.b);
+                for (int q = 0; q < C::kChunks; ++q)
+                  tma_load_3d_pair(sbp + q * C::kChunkBytes, mb, bar, tc.bj * kBN + rank * C::kBRows + q * C::kBK,
+                                   k0, tc.b);
+              } else {
+                tma_load_3d_pair(sbp, mb, bar, k0, tc.bj * kBN + rank * C::kBRows, tc.b);
+              }
             }
           }
-          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
+        __syncwarp();
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
-      if (*abort_p) {
-        // let loads already issued land before the CTA exits (bounded)
-        for (int s = 0; s < C::kStages; ++s)
-          (void)mbar_wait(&full_bar[s], phase ^ (s < stage ? 0u : 1u), nullptr, nullptr, 100000000ull);
-      }
+      if (!ok) break;
     }
+    if (*abort_p && (kCL == 1 || leader) && lane == 0) {
+      // let loads already issued land before the CTA exits (bounded)
+      for (int s = 0; s < C::kStages; ++s)
+        (void)mbar_wait(&full_bar[s], phase ^ (s < stage ? 0u : 1u), nullptr, nullptr, 100000000ull);
+    }
+    __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      const uint32_t idesc = make_idesc(C::kFormat, kBM, kBN, mn_b ? 1u : 0u);
+    if (leader) {
+      // ---------------- MMA issuer (the even CTA) ----------------
+      // converged warp; lane 0 issues the MMAs and the commits that track them
+      const uint32_t idesc = make_idesc(C::kFormat, kBM * kCL, kBN, mn_b ? 1u : 0u);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
-        const TileCoord tc = decode_tile(a, t);
+      for (int t = cluster_id; t < a.total_tiles; t += n_clusters) {
+        const TileCoord tc = decode_tile<kCL>(a, t, rank);
         const GemmGroup& G = a.g[tc.g];
         const int kblocks = (G.K + C::kBK - 1) / C::kBK;
-        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_p, status)) break;
+        const bool free_acc = mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_p, status);
+        if (!__all_sync(0xffffffffu, free_acc)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_p, status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (size_t)stage * C::kStage);
-          const uint32_t sb = sa + C::kParts * C::kA;
+          // the TMA bytes are visible to the tensor core once the barrier completes
+          const bool got = mbar_wait(&full_bar[stage], phase, abort_p, status);
+          if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(smem + (size_t)stage * C::kStage);
+            const uint32_t sb = sa + C::kParts * C::kA;
 #pragma unroll
-          for (int kk = 0; kk < C::kBK / C::kInstK; ++kk) {
-            const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = mn_b
-                                    ? smem_desc_sw128(sb + kk * C::kInstK * 128, C::kChunkBytes, 1024)
-                                    : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
-            if (kTF32) {
-              const uint64_t ad_lo = smem_desc_sw128(sa + C::kA + kk * 32, 16, 1024);
-              const uint64_t bd_lo = mn_b
-                                         ? smem_desc_sw128(sb + C::kB + kk * C::kInstK * 128, C::kChunkBytes, 1024)
-                                         : smem_desc_sw128(sb + C::kB + kk * 32, 16, 1024);
-              mma_tf32(d_tmem, ad_lo, bd, idesc, accumulate);
-              mma_tf32(d_tmem, ad, bd_lo, idesc, 1u);
-              mma_tf32(d_tmem, ad, bd, idesc, 1u);
-            } else {
-              mma_bf16(d_tmem, ad, bd, idesc, accumulate);
+            for (int kk = 0; kk < C::kBK / C::kInstK; ++kk) {
+              const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = mn_b ? smem_desc_sw128(sb + kk * C::kInstK * 128, C::kChunkBytes, 1024)
+                                       : smem_desc_sw128(sb + kk * 32, 16, 1024);
+              const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
+              if constexpr (kTF32) {
+                const uint64_t ad_lo = smem_desc_sw128(sa + C::kA + kk * 32, 16, 1024);
+                const uint64_t bd_lo = smem_desc_sw128(sb + C::kB + kk * 32, 16, 1024);  // tf32 B is K-major
+                mma<true, kCL>(d_tmem, ad_lo, bd, idesc, accumulate);
+                mma<true, kCL>(d_tmem, ad, bd_lo, idesc, 1u);
+                mma<true, kCL>(d_tmem, ad, bd, idesc, 1u);
+              } else {
+                mma<false, kCL>(d_tmem, ad, bd, idesc, accumulate);
+              }
             }
+            if constexpr (kCL > 1) mma_commit_multicast<kCL>(&empty_bar[stage], kPair);
+            else mma_commit<kCL>(&empty_bar[stage]);
           }
-          mma_commit(&empty_bar[stage]);
+          __syncwarp();
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&tfull_bar[acc]);
+        if (lane == 0) {
+          if constexpr (kCL > 1) mma_commit_multicast<kCL>(&tfull_bar[acc], kPair);
+          else mma_commit<kCL>(&tfull_bar[acc]);
+        }
+        __syncwarp();
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
-      // every MMA issued by this thread has completed before TMEM is freed
-      mma_commit(&drain_bar);
-      (void)mbar_wait(&drain_bar, 0u, nullptr, status);
+      // every MMA issued by lane 0 has completed before TMEM is freed
+      if (lane == 0) {
+        mma_commit<kCL>(&drain_bar);
+        (void)mbar_wait(&drain_bar, 0u, nullptr, status);
+      }
+      __syncwarp();
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..9 of both CTAs) ----------------
+    // warp w reads TMEM lanes 32*(w%4)..+31; the two warps of a lane quadrant
+    // split the 256 accumulator columns
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = quad * 32 + lane;
+    const uint32_t tempty_lead[2] = {kCL > 1 ? mapa_shared(&tempty_bar[0], 0) : 0u,
+                                     kCL > 1 ? mapa_shared(&tempty_bar[1], 0) : 0u};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < a.total_tiles; t += gridDim.x) {
-      const TileCoord tc = decode_tile(a, t);
+    for (int t = cluster_id; t < a.total_tiles; t += n_clusters) {
+      const TileCoord tc = decode_tile<kCL>(a, t, rank);
       const GemmGroup& G = a.g[tc.g];
+      const int64_t r = (int64_t)tc.bi * kBM + row_in_tile;
+      const int64_t mb = (int64_t)tc.b * G.c_mstride;
+      const int64_t ld = G.c_ld;
       // warp-uniform decision: tcgen05.ld below needs every lane of the warp
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_p, status);
       if (!__all_sync(0xffffffffu, got)) break;
@@ -379,11 +446,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
         if (mode == kUpdate) { alpha *= s; beta *= s; }
       }
       const bool sym = (mode != kUpdate);
-      const int64_t r = (int64_t)tc.bi * kBM + row_in_tile;
-      const int64_t mb = (int64_t)tc.b * G.c_mstride;
-      const int64_t ld = G.c_ld;
 #pragma unroll 1
-      for (int cc = 0; cc < kBN / 32; ++cc) {
+      for (int cc = half * (kBN / 64); cc < (half + 1) * (kBN / 64); ++cc) {
         float v[32];
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
         const int64_t c0 = (int64_t)tc.bj * kBN + cc * 32;
@@ -423,7 +487,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty_bar[acc]);
+      if constexpr (kCL == 1) {
+        mbar_arrive(&tempty_bar[acc]);
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_lead[acc]);  // release the accumulator to the MMA issuer
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -432,33 +501,66 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // neither CTA frees Tensor Memory or exits while the pair's MMAs or signals may still reach it
+  if constexpr (kCL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc<kCL>(tmem_base, kTmemCols);
   }
 }
 
-template <bool kTF32>
+template <bool kTF32, int kCL>
 cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<kTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<kTF32>::kSmem);
+  static int max_clusters = 0;
+  auto kernel = ns_gemm_kernel<kTF32, kCL>;
+  if (max_clusters == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cfg<kTF32, kCL>::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    max_clusters = num_sms / kCL;
+    if (kCL > 1) {
+      cudaLaunchConfig_t q = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = kCL;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      q.gridDim = dim3(num_sms / kCL * kCL);
+      q.blockDim = dim3(kThreadsG);
+      q.dynamicSmemBytes = Cfg<kTF32, kCL>::kSmem;
+      q.attrs = at;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) == cudaSuccess && n > 0) max_clusters = n;
+      cudaGetLastError();
+    }
   }
-  const int grid = a.total_tiles < num_sms ? a.total_tiles : num_sms;
-  ns_gemm_kernel<kTF32><<<grid, kThreadsG, Cfg<kTF32>::kSmem, s>>>(a);
-  return cudaGetLastError();
+  const int clusters = a.total_tiles < max_clusters ? a.total_tiles : max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(clusters * kCL);
+  cfg.blockDim = dim3(kThreadsG);
+  cfg.dynamicSmemBytes = Cfg<kTF32, kCL>::kSmem;
+  cfg.stream = s;
+  if (kCL > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes(bool tf32) { return tf32 ? Cfg<true>::kSmem : Cfg<false>::kSmem; }
+size_t gemm_smem_bytes(bool tf32) { return tf32 ? Cfg<true, 1>::kSmem : Cfg<false, 1>::kSmem; }
 
-cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, int cluster, cudaStream_t s) {
   if (a.total_tiles <= 0) return cudaSuccess;
-  return tf32 ? launch_impl<true>(a, num_sms, s) : launch_impl<false>(a, num_sms, s);
+  if (cluster == 2) return tf32 ? launch_impl<true, 2>(a, num_sms, s) : launch_impl<false, 2>(a, num_sms, s);
+  return tf32 ? launch_impl<true, 1>(a, num_sms, s) : launch_impl<false, 1>(a, num_sms, s);
 }
 
 }  // namespace muon

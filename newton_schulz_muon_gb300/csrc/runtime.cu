@@ -421,19 +421,33 @@ void make_apply_args(const muon_plan_t* p, const Bucket& b, F ptr, int final_buf
   a.flags = at<int32_t>(p, p->off_flags);
 }
 
-int64_t sym_tiles_per_mat(int64_t M) {
-  const int64_t tm = cdiv(M, kBM), tn = cdiv(M, kBN);
+// Row blocks of kBM * cluster rows touching the upper triangle, per 256-column block.
+int64_t sym_tiles_per_mat(int64_t M, int cluster) {
+  const int64_t rb = (int64_t)kBM * cluster;
+  const int64_t tm = cdiv(M, rb), tn = cdiv(M, kBN);
   int64_t total = 0;
-  for (int64_t bj = 0; bj < tn; ++bj) total += std::min(tm, (bj * kBN + kBN - 1) / kBM + 1);
+  for (int64_t bj = 0; bj < tn; ++bj) total += std::min(tm, (bj * kBN + kBN - 1) / rb + 1);
   return total;
 }
 
 muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st) {
   const muon_config& c = p->cfg;
   const bool tf32 = c.ns_precision == MUON_NS_TF32X3;
+  // pairs of CTAs share the B operand unless a group is a single 128-row tile high
+  int cluster = 2;
+  for (const BGroup& g : b.groups)
+    if (g.m <= kBM) cluster = 1;
   for (int it = 0; it < ns_steps; ++it) {
     const int cur = it & 1, nxt = cur ^ 1;
     for (int mode = kGram; mode <= kUpdate; ++mode) {
+      // deal the longest reductions first: groups by K (n for GRAM, m otherwise), descending
+      std::vector<size_t> order(b.groups.size());
+      for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+      std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) {
+        const int64_t kx = mode == kGram ? b.groups[x].n : b.groups[x].m;
+        const int64_t ky = mode == kGram ? b.groups[y].n : b.groups[y].m;
+        return kx > ky;
+      });
       GemmArgs ga;
       std::memset(&ga, 0, sizeof(ga));
       ga.mode = mode;
@@ -445,7 +459,7 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
       ga.status = at<DeviceStatus>(p, p->off_status);
       int tiles = 0;
       for (size_t gi = 0; gi < b.groups.size(); ++gi) {
-        const BGroup& g = b.groups[gi];
+        const BGroup& g = b.groups[order[gi]];
         GemmGroup& G = ga.g[gi];
         uint8_t* ns = p->ws + p->off_ns;
         G.count = (int32_t)g.count;
@@ -479,14 +493,14 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
           G.c_ld = g.ld_n; G.c_mstride = g.m * g.ld_n;
           G.M = (int32_t)g.m; G.N = (int32_t)g.n; G.K = (int32_t)g.m;
         }
-        G.tiles_m = (int32_t)cdiv(G.M, kBM);
+        G.tiles_m = (int32_t)cdiv(G.M, (int64_t)kBM * cluster);
         G.tiles_n = (int32_t)cdiv(G.N, kBN);
-        G.tiles_per_mat = mode == kUpdate ? G.tiles_m * G.tiles_n : (int32_t)sym_tiles_per_mat(G.M);
+        G.tiles_per_mat = mode == kUpdate ? G.tiles_m * G.tiles_n : (int32_t)sym_tiles_per_mat(G.M, cluster);
         G.tile0 = tiles;
         tiles += G.tiles_per_mat * G.count;
       }
       ga.total_tiles = tiles;
-      cudaError_t e = launch_gemm(ga, p->num_sms, tf32, st);
+      cudaError_t e = launch_gemm(ga, p->num_sms, tf32, cluster, st);
       if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
     }
   }
