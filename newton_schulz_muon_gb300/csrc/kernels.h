@@ -124,6 +124,11 @@ struct GemmArgs {
   float alpha, beta;      // GRAM: 1, -; POLY: c, b; UPDATE: 1, a
   const float* scale;     // per bucket-local matrix
   DeviceStatus* status;
+  // tile schedule: cluster c runs tiles sched_units[sched_off[c] .. sched_off[c+1])
+  const int32_t* sched_off;
+  const int32_t* sched_units;
+  int32_t n_clusters;
+  int32_t pad2_;
 };
 
 // GEMM tile shape (bf16): 128 x 256 outputs per CTA, 64-deep k blocks.
@@ -137,6 +142,9 @@ cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t s);
 // cluster: 1, or 2 (pairs of vertically adjacent tiles share the B operand);
 // GemmGroup::tiles_m counts row blocks of kBM * cluster rows.
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, int cluster, cudaStream_t s);
+// Clusters of the GEMM kernel that can be resident at once on this device
+// (a.n_clusters must not exceed it).
+int gemm_max_clusters(bool tf32, int cluster, int num_sms);
 size_t gemm_smem_bytes(bool tf32);
 
 // Records `msg` as the calling thread's muon_last_error text and returns `s`.

@@ -33,8 +33,8 @@
 //                   tcgen05.ld (two warps per lane quadrant, 128 columns each),
 //                   applies alpha/beta, converts and stores.
 // Tiles of all same-shape groups of a micro-bucket (and of all its matrices) are
-// numbered in one space and dealt round-robin to the CTAs (groups ordered by
-// reduction length, longest first).
+// numbered in one space; a host-computed longest-processing-time schedule gives
+// each cluster its list of tiles.
 //
 // kCL = 2 (the default for m > 128): a cluster of two CTAs on two SMs computes a
 // 256 x 256 tile with one tcgen05.mma.cta_group::2 (M=256, N=256) issued by the
@@ -253,7 +253,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
   const int rank = kCL > 1 ? (int)cluster_ctarank() : 0;
   const bool leader = rank == 0;
   const int cluster_id = blockIdx.x / kCL;
-  const int n_clusters = gridDim.x / kCL;
   constexpr uint16_t kPair = (1u << kCL) - 1u;
   unsigned* status = &a.status->flags;
   volatile int* abort_p = &abort_flag;
@@ -300,7 +299,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     // Issuing from a lone lane of a diverged warp is several times slower.
     int stage = 0;
     uint32_t phase = 0;
-    for (int t = cluster_id; t < a.total_tiles; t += n_clusters) {
+    for (int si = a.sched_off[cluster_id]; si < a.sched_off[cluster_id + 1]; ++si) {
+      const int t = a.sched_units[si];
       const TileCoord tc = decode_tile<kCL>(a, t, rank);
       const GemmGroup& G = a.g[tc.g];
       const int kblocks = (G.K + C::kBK - 1) / C::kBK;
@@ -364,7 +364,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int t = cluster_id; t < a.total_tiles; t += n_clusters) {
+      for (int si = a.sched_off[cluster_id]; si < a.sched_off[cluster_id + 1]; ++si) {
+      const int t = a.sched_units[si];
         const TileCoord tc = decode_tile<kCL>(a, t, rank);
         const GemmGroup& G = a.g[tc.g];
         const int kblocks = (G.K + C::kBK - 1) / C::kBK;
@@ -429,7 +430,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
                                      kCL > 1 ? mapa_shared(&tempty_bar[1], 0) : 0u};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = cluster_id; t < a.total_tiles; t += n_clusters) {
+    for (int si = a.sched_off[cluster_id]; si < a.sched_off[cluster_id + 1]; ++si) {
+      const int t = a.sched_units[si];
       const TileCoord tc = decode_tile<kCL>(a, t, rank);
       const GemmGroup& G = a.g[tc.g];
       const int64_t r = (int64_t)tc.bi * kBM + row_in_tile;
@@ -510,35 +512,45 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
 }
 
 template <bool kTF32, int kCL>
-cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
-  static int max_clusters = 0;
+int max_clusters_impl(int num_sms) {
+  static int cached = 0;
+  if (cached) return cached;
   auto kernel = ns_gemm_kernel<kTF32, kCL>;
-  if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<kTF32, kCL>::kSmem);
-    if (e != cudaSuccess) return e;
-    max_clusters = num_sms / kCL;
-    if (kCL > 1) {
-      cudaLaunchConfig_t q = {};
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = kCL;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      q.gridDim = dim3(num_sms / kCL * kCL);
-      q.blockDim = dim3(kThreadsG);
-      q.dynamicSmemBytes = Cfg<kTF32, kCL>::kSmem;
-      q.attrs = at;
-      q.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) == cudaSuccess && n > 0) max_clusters = n;
-      cudaGetLastError();
-    }
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<kTF32, kCL>::kSmem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
   }
-  const int clusters = a.total_tiles < max_clusters ? a.total_tiles : max_clusters;
+  int n = num_sms / kCL;
+  if (kCL > 1) {
+    cudaLaunchConfig_t q = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kCL;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    q.gridDim = dim3(num_sms / kCL * kCL);
+    q.blockDim = dim3(kThreadsG);
+    q.dynamicSmemBytes = Cfg<kTF32, kCL>::kSmem;
+    q.attrs = at;
+    q.numAttrs = 1;
+    int m = 0;
+    if (cudaOccupancyMaxActiveClusters(&m, kernel, &q) == cudaSuccess && m > 0) n = m;
+    cudaGetLastError();
+  }
+  cached = n;
+  return n;
+}
+
+template <bool kTF32, int kCL>
+cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
+  const int maxc = max_clusters_impl<kTF32, kCL>(num_sms);
+  if (maxc <= 0) return cudaErrorInvalidConfiguration;
+  if (a.n_clusters <= 0 || a.n_clusters > maxc) return cudaErrorInvalidValue;
+  auto kernel = ns_gemm_kernel<kTF32, kCL>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(clusters * kCL);
+  cfg.gridDim = dim3(a.n_clusters * kCL);
   cfg.blockDim = dim3(kThreadsG);
   cfg.dynamicSmemBytes = Cfg<kTF32, kCL>::kSmem;
   cfg.stream = s;
@@ -556,6 +568,11 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
 }  // namespace
 
 size_t gemm_smem_bytes(bool tf32) { return tf32 ? Cfg<true, 1>::kSmem : Cfg<false, 1>::kSmem; }
+
+int gemm_max_clusters(bool tf32, int cluster, int num_sms) {
+  if (cluster == 2) return tf32 ? max_clusters_impl<true, 2>(num_sms) : max_clusters_impl<false, 2>(num_sms);
+  return tf32 ? max_clusters_impl<true, 1>(num_sms) : max_clusters_impl<false, 1>(num_sms);
+}
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, int cluster, cudaStream_t s) {
   if (a.total_tiles <= 0) return cudaSuccess;

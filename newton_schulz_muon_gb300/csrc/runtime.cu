@@ -98,6 +98,18 @@ struct Bucket {
   int n_runs = 0;
   int64_t prep_tiles = 0;
   size_t ns_bytes = 0;
+  // per GEMM phase: tile schedule (byte offset in the schedule region, clusters)
+  size_t sched_off[3] = {0, 0, 0};
+  int32_t sched_clusters[3] = {0, 0, 0};
+};
+
+// Shape of one grouped GEMM launch of a bucket: cluster size, groups in launch
+// order (longest reduction first), tiles per matrix and k blocks per group.
+struct LaunchShape {
+  int cluster = 1;
+  std::vector<size_t> order;
+  std::vector<int64_t> tiles_per_mat, kblocks, M, N, K;
+  int64_t total = 0;
 };
 
 struct BucketEvents {
@@ -116,6 +128,7 @@ struct muon_plan_s {
   int64_t n_matrices = 0;
   // layout
   size_t off_status = 0, off_scale = 0, off_flags = 0, off_partials = 0, off_ns = 0, off_stage = 0;
+  size_t off_sched = 0, sched_bytes = 0;
   size_t ns_bytes = 0, slot_bytes = 0, ws_bytes = 0;
   int n_slots = 0;
   int64_t max_mats = 0, max_tiles = 0, max_elems = 0;
@@ -206,6 +219,88 @@ void layout_bucket(Bucket& b, const muon_config& cfg) {
 
 int64_t tiles_of(int64_t rows, int64_t cols) { return cdiv(rows, kPrepTile) * cdiv(cols, kPrepTile); }
 
+// Row blocks of kBM * cluster rows touching the upper triangle, per 256-column block.
+int64_t sym_tiles_per_mat(int64_t M, int cluster) {
+  const int64_t rb = (int64_t)kBM * cluster;
+  const int64_t tm = cdiv(M, rb), tn = cdiv(M, kBN);
+  int64_t total = 0;
+  for (int64_t bj = 0; bj < tn; ++bj) total += std::min(tm, (bj * kBN + kBN - 1) / rb + 1);
+  return total;
+}
+
+LaunchShape launch_shape(const Bucket& b, int mode, bool tf32) {
+  LaunchShape L;
+  L.cluster = 2;  // pairs of CTAs share the B operand unless a group is one 128-row tile high
+  for (const BGroup& g : b.groups)
+    if (g.m <= kBM) L.cluster = 1;
+  L.order.resize(b.groups.size());
+  for (size_t i = 0; i < L.order.size(); ++i) L.order[i] = i;
+  std::stable_sort(L.order.begin(), L.order.end(), [&](size_t x, size_t y) {
+    const int64_t kx = mode == kGram ? b.groups[x].n : b.groups[x].m;
+    const int64_t ky = mode == kGram ? b.groups[y].n : b.groups[y].m;
+    return kx > ky;
+  });
+  const int64_t bk = tf32 ? 32 : 64;
+  for (size_t gi : L.order) {
+    const BGroup& g = b.groups[gi];
+    const int64_t M = g.m, N = mode == kUpdate ? g.n : g.m, K = mode == kGram ? g.n : g.m;
+    const int64_t tpm = mode == kUpdate ? cdiv(M, (int64_t)kBM * L.cluster) * cdiv(N, kBN)
+                                        : sym_tiles_per_mat(M, L.cluster);
+    L.M.push_back(M);
+    L.N.push_back(N);
+    L.K.push_back(K);
+    L.tiles_per_mat.push_back(tpm);
+    L.kblocks.push_back(cdiv(K, bk));
+    L.total += tpm * g.count;
+  }
+  return L;
+}
+
+// Longest-processing-time assignment of the launch's tiles to `clusters`
+// clusters: tiles by cost (k blocks plus an epilogue allowance), longest first,
+// each to the least-loaded cluster.  Output: offsets[clusters + 1], units[total].
+void lpt_schedule(const Bucket& b, const LaunchShape& L, int mode, int clusters, std::vector<int32_t>& out) {
+  const int64_t epi = mode == kGram ? 2 : 3;
+  std::vector<std::pair<int64_t, int32_t>> units;  // (cost, tile)
+  units.reserve(L.total);
+  int64_t t = 0;
+  for (size_t i = 0; i < L.order.size(); ++i) {
+    const int64_t n = L.tiles_per_mat[i] * b.groups[L.order[i]].count;
+    for (int64_t j = 0; j < n; ++j) units.emplace_back(L.kblocks[i] + epi, (int32_t)(t + j));
+    t += n;
+  }
+  std::stable_sort(units.begin(), units.end(),
+                   [](const std::pair<int64_t, int32_t>& x, const std::pair<int64_t, int32_t>& y) {
+                     return x.first > y.first;
+                   });
+  std::vector<std::vector<int32_t>> per(clusters);
+  // min-heap on (load, cluster id): ties go to the lowest id, so the result is deterministic
+  std::vector<std::pair<int64_t, int32_t>> heap;
+  for (int c = 0; c < clusters; ++c) heap.emplace_back(0, c);
+  auto cmp = [](const std::pair<int64_t, int32_t>& x, const std::pair<int64_t, int32_t>& y) {
+    return x.first != y.first ? x.first > y.first : x.second > y.second;
+  };
+  std::make_heap(heap.begin(), heap.end(), cmp);
+  for (const auto& u : units) {
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    auto& top = heap.back();
+    per[top.second].push_back(u.second);
+    top.first += u.first;
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  }
+  out.clear();
+  out.reserve(clusters + 1 + units.size());
+  int32_t off = 0;
+  for (int c = 0; c < clusters; ++c) {
+    out.push_back(off);
+    off += (int32_t)per[c].size();
+  }
+  out.push_back(off);
+  for (int c = 0; c < clusters; ++c) out.insert(out.end(), per[c].begin(), per[c].end());
+}
+
+constexpr int kMaxClusters = 256;  // bound on resident clusters, for the schedule region's size
+
 muon_status build_plan(muon_plan_t* p, const muon_shape* shapes, int32_t n, const int32_t* labels) {
   std::map<std::tuple<int, int64_t, int64_t>, int> gid;
   for (int i = 0; i < n; ++i) {
@@ -295,6 +390,17 @@ muon_status build_plan(muon_plan_t* p, const muon_shape* shapes, int32_t n, cons
   p->off_partials = off; off = align_up(off + (size_t)p->max_tiles * 4, kAlign);
   p->off_ns = off; off = align_up(off + ns_max, kAlign);
   p->ns_bytes = ns_max;
+  // tile schedules, one per bucket and GEMM phase: offsets (clusters + 1) and tiles
+  size_t sched = 0;
+  const bool tf32 = p->cfg.ns_precision == MUON_NS_TF32X3;
+  for (Bucket& b : p->buckets)
+    for (int mode = kGram; mode <= kUpdate; ++mode) {
+      b.sched_off[mode] = sched;
+      sched += (size_t)(launch_shape(b, mode, tf32).total + kMaxClusters + 1) * sizeof(int32_t);
+      sched = align_up(sched, 256);
+    }
+  p->off_sched = off; off = align_up(off + sched, kAlign);
+  p->sched_bytes = sched;
   if (p->cfg.offload) {
     p->n_slots = std::max(1, std::min(2, (int)p->cfg.max_inflight)) + 1;
     p->slot_bytes = align_up((size_t)p->max_elems * grad_size(p->cfg), kAlign) +
@@ -421,33 +527,15 @@ void make_apply_args(const muon_plan_t* p, const Bucket& b, F ptr, int final_buf
   a.flags = at<int32_t>(p, p->off_flags);
 }
 
-// Row blocks of kBM * cluster rows touching the upper triangle, per 256-column block.
-int64_t sym_tiles_per_mat(int64_t M, int cluster) {
-  const int64_t rb = (int64_t)kBM * cluster;
-  const int64_t tm = cdiv(M, rb), tn = cdiv(M, kBN);
-  int64_t total = 0;
-  for (int64_t bj = 0; bj < tn; ++bj) total += std::min(tm, (bj * kBN + kBN - 1) / rb + 1);
-  return total;
-}
-
 muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st) {
   const muon_config& c = p->cfg;
   const bool tf32 = c.ns_precision == MUON_NS_TF32X3;
-  // pairs of CTAs share the B operand unless a group is a single 128-row tile high
-  int cluster = 2;
-  for (const BGroup& g : b.groups)
-    if (g.m <= kBM) cluster = 1;
+  LaunchShape shapes[3];
+  for (int mode = kGram; mode <= kUpdate; ++mode) shapes[mode] = launch_shape(b, mode, tf32);
   for (int it = 0; it < ns_steps; ++it) {
     const int cur = it & 1, nxt = cur ^ 1;
     for (int mode = kGram; mode <= kUpdate; ++mode) {
-      // deal the longest reductions first: groups by K (n for GRAM, m otherwise), descending
-      std::vector<size_t> order(b.groups.size());
-      for (size_t i = 0; i < order.size(); ++i) order[i] = i;
-      std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) {
-        const int64_t kx = mode == kGram ? b.groups[x].n : b.groups[x].m;
-        const int64_t ky = mode == kGram ? b.groups[y].n : b.groups[y].m;
-        return kx > ky;
-      });
+      const LaunchShape& L = shapes[mode];
       GemmArgs ga;
       std::memset(&ga, 0, sizeof(ga));
       ga.mode = mode;
@@ -457,9 +545,13 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
       ga.beta = mode == kPoly ? c.ns_b : (mode == kUpdate ? c.ns_a : 0.0f);
       ga.scale = at<float>(p, p->off_scale);
       ga.status = at<DeviceStatus>(p, p->off_status);
+      const int32_t* sched = reinterpret_cast<const int32_t*>(p->ws + p->off_sched + b.sched_off[mode]);
+      ga.n_clusters = b.sched_clusters[mode];
+      ga.sched_off = sched;
+      ga.sched_units = sched + ga.n_clusters + 1;
       int tiles = 0;
-      for (size_t gi = 0; gi < b.groups.size(); ++gi) {
-        const BGroup& g = b.groups[order[gi]];
+      for (size_t gi = 0; gi < L.order.size(); ++gi) {
+        const BGroup& g = b.groups[L.order[gi]];
         GemmGroup& G = ga.g[gi];
         uint8_t* ns = p->ws + p->off_ns;
         G.count = (int32_t)g.count;
@@ -471,14 +563,12 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
           G.c_hi = ns + g.off_a; G.c_lo = lo(g.off_a_lo);
           G.d_hi = nullptr; G.d_lo = nullptr;
           G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
-          G.M = (int32_t)g.m; G.N = (int32_t)g.m; G.K = (int32_t)g.n;
         } else if (mode == kPoly) {
           G.map_a = g.ka; G.map_b = g.ka;
           if (tf32) { G.map_a_lo = g.ka_lo; G.map_b_lo = g.ka_lo; }
           G.c_hi = ns + g.off_b; G.c_lo = lo(g.off_b_lo);
           G.d_hi = ns + g.off_a; G.d_lo = lo(g.off_a_lo);
           G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
-          G.M = (int32_t)g.m; G.N = (int32_t)g.m; G.K = (int32_t)g.m;
         } else {
           G.map_a = g.kb; G.map_b = g.mx[cur];
           if (tf32) {
@@ -491,16 +581,18 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
           G.c_hi = ns + g.off_x[nxt]; G.c_lo = lo(g.off_x_lo[nxt]);
           G.d_hi = ns + g.off_x[cur]; G.d_lo = lo(g.off_x_lo[cur]);
           G.c_ld = g.ld_n; G.c_mstride = g.m * g.ld_n;
-          G.M = (int32_t)g.m; G.N = (int32_t)g.n; G.K = (int32_t)g.m;
         }
-        G.tiles_m = (int32_t)cdiv(G.M, (int64_t)kBM * cluster);
-        G.tiles_n = (int32_t)cdiv(G.N, kBN);
-        G.tiles_per_mat = mode == kUpdate ? G.tiles_m * G.tiles_n : (int32_t)sym_tiles_per_mat(G.M, cluster);
+        G.M = (int32_t)L.M[gi];
+        G.N = (int32_t)L.N[gi];
+        G.K = (int32_t)L.K[gi];
+        G.tiles_m = (int32_t)cdiv(L.M[gi], (int64_t)kBM * L.cluster);
+        G.tiles_n = (int32_t)cdiv(L.N[gi], kBN);
+        G.tiles_per_mat = (int32_t)L.tiles_per_mat[gi];
         G.tile0 = tiles;
         tiles += G.tiles_per_mat * G.count;
       }
       ga.total_tiles = tiles;
-      cudaError_t e = launch_gemm(ga, p->num_sms, tf32, cluster, st);
+      cudaError_t e = launch_gemm(ga, p->num_sms, tf32, L.cluster, st);
       if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
     }
   }
@@ -678,6 +770,23 @@ muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes
       }
       if (!ok) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled rejected a workspace tensor map");
     }
+  }
+  {
+    // tile schedules for this device's number of resident clusters
+    std::vector<int32_t> host(p->sched_bytes / sizeof(int32_t), 0), one;
+    for (Bucket& b : p->buckets)
+      for (int mode = kGram; mode <= kUpdate; ++mode) {
+        const LaunchShape L = launch_shape(b, mode, tf32);
+        int clusters = gemm_max_clusters(tf32, L.cluster, p->num_sms);
+        if (clusters <= 0 || clusters > kMaxClusters)
+          return fail(MUON_ERR_CUDA, "could not size the GEMM grid (%d resident clusters)", clusters);
+        if (L.total < clusters) clusters = (int)std::max<int64_t>(L.total, 1);
+        lpt_schedule(b, L, mode, clusters, one);
+        std::copy(one.begin(), one.end(), host.begin() + b.sched_off[mode] / sizeof(int32_t));
+        b.sched_clusters[mode] = clusters;
+      }
+    e = cudaMemcpy(p->ws + p->off_sched, host.data(), p->sched_bytes, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
   }
   if (!p->h2d_stream) {
     e = cudaStreamCreateWithFlags(&p->h2d_stream, cudaStreamNonBlocking);
