@@ -128,7 +128,10 @@ struct GemmArgs {
   const int32_t* sched_off;
   const int32_t* sched_units;
   int32_t n_clusters;
-  int32_t pad2_;
+  // last UPDATE of a step: apply the weight update (or emit U') from the
+  // epilogue instead of storing X; `apply` describes the weights per matrix run
+  int32_t fuse_apply;
+  ApplyArgs apply;
 };
 
 // GEMM tile shape (bf16): 128 x 256 outputs per CTA, 64-deep k blocks.

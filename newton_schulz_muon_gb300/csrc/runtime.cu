@@ -527,7 +527,8 @@ void make_apply_args(const muon_plan_t* p, const Bucket& b, F ptr, int final_buf
   a.flags = at<int32_t>(p, p->off_flags);
 }
 
-muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st) {
+muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st,
+                       const ApplyArgs* fused = nullptr) {
   const muon_config& c = p->cfg;
   const bool tf32 = c.ns_precision == MUON_NS_TF32X3;
   LaunchShape shapes[3];
@@ -547,6 +548,10 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
       ga.status = at<DeviceStatus>(p, p->off_status);
       const int32_t* sched = reinterpret_cast<const int32_t*>(p->ws + p->off_sched + b.sched_off[mode]);
       ga.n_clusters = b.sched_clusters[mode];
+      if (fused && mode == kUpdate && it == ns_steps - 1) {
+        ga.fuse_apply = 1;
+        ga.apply = *fused;
+      }
       ga.sched_off = sched;
       ga.sched_units = sched + ga.n_clusters + 1;
       int tiles = 0;
@@ -852,13 +857,16 @@ muon_status muon_step(muon_plan_t* p, void* const* params, const void* const* gr
     e = launch_norm(pa, st);
     if (e != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
     if (timing) cudaEventRecord(p->events[bi].prep, st);
-    muon_status s = enqueue_ns(p, b, ns_steps, st);
-    if (s != MUON_OK) return s;
-    if (timing) cudaEventRecord(p->events[bi].ns, st);
+    // the weight update runs in the last UPDATE's epilogue; with no iteration, in its own kernel
     ApplyArgs aa;
     make_apply_args(p, b, ptrs, ns_steps & 1, lr, wd, 0, ns_steps, aa);
-    e = launch_apply(aa, st);
-    if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+    muon_status s = enqueue_ns(p, b, ns_steps, st, ns_steps > 0 ? &aa : nullptr);
+    if (s != MUON_OK) return s;
+    if (timing) cudaEventRecord(p->events[bi].ns, st);
+    if (ns_steps == 0) {
+      e = launch_apply(aa, st);
+      if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+    }
     if (timing) cudaEventRecord(p->events[bi].apply, st);
   }
   if (timing) cudaEventRecord(p->step_end, st);
@@ -944,12 +952,12 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
     if (timing) cudaEventRecord(p->events[bi].prep, cs);  // marks compute start for this bucket
     if ((e = launch_prep(pa, cs)) != cudaSuccess) return cuda_fail(e, "momentum_prep launch");
     if ((e = launch_norm(pa, cs)) != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
-    muon_status s = enqueue_ns(p, b, ns_steps, cs);
-    if (s != MUON_OK) return s;
-    if (timing) cudaEventRecord(p->events[bi].ns, cs);
     ApplyArgs aa;
     make_apply_args(p, b, stage_ptrs, ns_steps & 1, 0.f, 0.f, 1, ns_steps, aa);
-    if ((e = launch_apply(aa, cs)) != cudaSuccess) return cuda_fail(e, "emit launch");
+    muon_status s = enqueue_ns(p, b, ns_steps, cs, ns_steps > 0 ? &aa : nullptr);
+    if (s != MUON_OK) return s;
+    if (timing) cudaEventRecord(p->events[bi].ns, cs);
+    if (ns_steps == 0 && (e = launch_apply(aa, cs)) != cudaSuccess) return cuda_fail(e, "emit launch");
     cudaEventRecord(p->slot_comp[slot], cs);
     if (timing) cudaEventRecord(p->events[bi].apply, cs);
     // device -> host writeback on the side stream
