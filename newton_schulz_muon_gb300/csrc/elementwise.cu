@@ -8,7 +8,7 @@
 //    Sources: "Muon Optimizer + FSDP", section 背景 (M_t = momentum_update(grad)
 //    feeds NewtonSchulz); section 内存控制方案 item 4 (bf16 Newton-Schulz buffers,
 //    normalisation scalars kept in fp32).
-//  * norm_finalize: per matrix, sums its tile partials in a fixed order (fp64),
+//  * norm_finalize: per matrix (one block), sums its tile partials in a fixed order (fp64),
 //    and stores s = 1 / (||V||_F + eps) and a non-finite flag.  s is folded into
 //    the first Newton-Schulz iteration's GEMM epilogues instead of rescaling X0.
 //  * apply: W <- W - lr (sqrt(max(1, rows/cols)) U + wd W), un-transposing U
@@ -118,35 +118,47 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
   const bool full = (tile.r0 + kT <= rows) && (tile.c0 + kT <= cols);
   const bool vec = full && ((cols & 3) == 0) && ((s.stride & 3) == 0);
   float* mrow = s.m + base;
+  if (vec) {
+    // all loads of the thread's 4 x 4 elements first, then arithmetic, then stores
+    float4 mv[4];
+    float gv[4][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int64_t r = tile.r0 + ty + 16 * k;
-    const int64_t c = tile.c0 + 4 * tx;
-    if (vec) {
-      const int64_t off = r * cols + c;
-      float4 mv = *reinterpret_cast<const float4*>(mrow + off);
-      float gv[4];
+    for (int k = 0; k < 4; ++k) {
+      const int64_t off = (tile.r0 + ty + 16 * k) * cols + tile.c0 + 4 * tx;
+      mv[k] = __ldcs(reinterpret_cast<const float4*>(mrow + off));
       if (a.grad_dtype == 1) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(
-            reinterpret_cast<const __nv_bfloat16*>(s.g) + base + off);
+        const uint2 raw = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(s.g) + base + off));
         const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
         const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-        gv[0] = __low2float(g01); gv[1] = __high2float(g01);
-        gv[2] = __low2float(g23); gv[3] = __high2float(g23);
+        gv[k][0] = __low2float(g01); gv[k][1] = __high2float(g01);
+        gv[k][2] = __low2float(g23); gv[k][3] = __high2float(g23);
       } else {
-        const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(s.g) + base + off);
-        gv[0] = f.x; gv[1] = f.y; gv[2] = f.z; gv[3] = f.w;
+        const float4 f = __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(s.g) + base + off));
+        gv[k][0] = f.x; gv[k][1] = f.y; gv[k][2] = f.z; gv[k][3] = f.w;
       }
-      float mo[4] = {mv.x, mv.y, mv.z, mv.w};
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float mo[4] = {mv[k].x, mv[k].y, mv[k].z, mv[k].w};
       float mn[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        mn[j] = dot2_accurate(mu, mo[j], omu, gv[j]);
-        v[k][j] = a.nesterov ? __fmaf_rn(mu, mn[j], __fmul_rn(omu, gv[j])) : mn[j];
+        mn[j] = dot2_accurate(mu, mo[j], omu, gv[k][j]);
+        v[k][j] = a.nesterov ? __fmaf_rn(mu, mn[j], __fmul_rn(omu, gv[k][j])) : mn[j];
         sumsq = __fmaf_rn(v[k][j], v[k][j], sumsq);
       }
-      *reinterpret_cast<float4*>(mrow + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
-    } else {
+      mv[k] = make_float4(mn[0], mn[1], mn[2], mn[3]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t off = (tile.r0 + ty + 16 * k) * cols + tile.c0 + 4 * tx;
+      __stcs(reinterpret_cast<float4*>(mrow + off), mv[k]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t r = tile.r0 + ty + 16 * k;
+      const int64_t c = tile.c0 + 4 * tx;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         v[k][j] = 0.f;
@@ -236,24 +248,31 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
   }
 }
 
-// One warp per matrix: fixed-order fp64 sum of its tile partials.
-__global__ void norm_finalize_kernel(const __grid_constant__ PrepArgs a) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= a.n_mats) return;
+// One block per matrix: each thread sums a fixed strided subset of the matrix's
+// tile partials in fp64, then a fixed-shape tree combines them (deterministic).
+__global__ void __launch_bounds__(256) norm_finalize_kernel(const __grid_constant__ PrepArgs a) {
+  __shared__ double red[256];
+  const int mat = blockIdx.x;
+  if (mat >= a.n_mats) return;
   int si = 0;
   for (int i = 1; i < a.n_segs; ++i)
-    if (a.seg[i].mat0 <= warp) si = i;
+    if (a.seg[i].mat0 <= mat) si = i;
   const PrepSeg& s = a.seg[si];
-  const int64_t first = s.block0 + (int64_t)(warp - s.mat0) * s.tiles_per_mat;
+  const int64_t first = s.block0 + (int64_t)(mat - s.mat0) * s.tiles_per_mat;
   double acc = 0.0;
-  for (int64_t i = lane; i < s.tiles_per_mat; i += 32) acc += (double)a.partials[first + i];
+  for (int64_t i = threadIdx.x; i < s.tiles_per_mat; i += 256) acc += (double)a.partials[first + i];
+  red[threadIdx.x] = acc;
+  __syncthreads();
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    const bool finite = isfinite(acc);
-    a.scale[warp] = finite ? (float)(1.0 / (sqrt(acc) + (double)a.eps)) : 0.f;
-    a.flags[warp] = finite ? 0 : 1;
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double tot = red[0];
+    const bool finite = isfinite(tot);
+    a.scale[mat] = finite ? (float)(1.0 / (sqrt(tot) + (double)a.eps)) : 0.f;
+    a.flags[mat] = finite ? 0 : 1;
     if (!finite) atomicAdd(&a.status->nonfinite, 1u);
   }
 }
@@ -377,9 +396,7 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
 
 cudaError_t launch_norm(const PrepArgs& a, cudaStream_t s) {
   if (a.n_mats <= 0) return cudaSuccess;
-  const int threads = 256;
-  const int blocks = (a.n_mats * 32 + threads - 1) / threads;
-  norm_finalize_kernel<<<blocks, threads, 0, s>>>(a);
+  norm_finalize_kernel<<<a.n_mats, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
