@@ -204,6 +204,32 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def workload_spec(name):
+    """Tensors (rows, cols, count), dtypes, distributions and bucket cap of a workload."""
+    import synth
+    if name == "layer":
+        return dict(desc=WORKLOAD, tensors=[(r, c, 1) for _, r, c in QWEN3_4B_LAYER], g_dtype=synth.BF16,
+                    g_sigma=G_SIGMA, w_dtype=synth.F32, w_sigma=W_SIGMA, m_sigma=M_SIGMA, cap=512 << 20)
+    if name == "single":
+        return dict(desc="single 256x512 matrix: W fp32 N(0,0.02), G fp32 N(0,1), M zero; mu 0.95 Nesterov, "
+                         "lr 0.02, wd 0, 5 NS iterations", tensors=[(256, 512, 1)], g_dtype=synth.F32,
+                    g_sigma=1.0, w_dtype=synth.F32, w_sigma=W_SIGMA, m_sigma=0.0, cap=512 << 20)
+    if name == "heads":
+        return dict(desc="per-head Muon on fused interleaved QKV [6144, 2560] x 36 layers: 1728 logical 128x2560 "
+                         "matrices in one batch; G bf16 N(0,1e-3), M and W fp32 N(0,0.02)",
+                    tensors=[(128, 2560, 48)] * 36, g_dtype=synth.BF16, g_sigma=G_SIGMA, w_dtype=synth.F32,
+                    w_sigma=W_SIGMA, m_sigma=M_SIGMA, cap=0)
+    if name == "experts":
+        t = []
+        for _ in range(48):
+            t += [(768, 2048, 128), (768, 2048, 128), (2048, 768, 128)]
+        return dict(desc="MoE experts of a 30B-A3B shape: gate/up [128,768,2048], down [128,2048,768] x 48 layers "
+                         "(18432 matrices); G bf16 N(0,1e-3), M zero, W bf16 N(0,0.02); 512 MiB buckets",
+                    tensors=t, g_dtype=synth.BF16, g_sigma=G_SIGMA, w_dtype=synth.BF16, w_sigma=W_SIGMA,
+                    m_sigma=0.0, cap=512 << 20)
+    raise ValueError(name)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -221,24 +247,29 @@ def run_gpu(args):
     import newton_schulz_muon_gb300 as nsm
     import synth
 
-    shapes = [(r, c, 1, 0) for _, r, c in QWEN3_4B_LAYER]
-    cfg = nsm.muon_config_default(timing=1)
-    plan = nsm.muon_plan(shapes, bucket_cap_bytes=512 << 20, config=cfg)
+    spec = workload_spec(args.workload)
+    tensors = spec["tensors"]
+    shapes = [(r, c, k, 0) for (r, c, k) in tensors]
+    cfg = nsm.muon_config_default(timing=1, grad_dtype=spec["g_dtype"], param_dtype=spec["w_dtype"])
+    plan = nsm.muon_plan(shapes, bucket_cap_bytes=spec["cap"], config=cfg)
     info = nsm.muon_get_plan_info(plan)
     ws = nsm.allocate_workspace(plan)
+    tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16}
     W, M, G = [], [], []
-    for i, (_, r, c) in enumerate(QWEN3_4B_LAYER):
-        w = torch.empty((r, c), dtype=torch.float32, device="cuda")
-        mm = torch.empty((r, c), dtype=torch.float32, device="cuda")
-        g = torch.empty((r, c), dtype=torch.bfloat16, device="cuda")
-        synth.fill_normal_cuda(w, synth.SEED, synth.stream_id(i, synth.ROLE_W), 0, W_SIGMA)
-        synth.fill_normal_cuda(mm, synth.SEED, synth.stream_id(i, synth.ROLE_M), 0, M_SIGMA)
-        synth.fill_normal_cuda(g, synth.SEED, synth.stream_id(i, synth.ROLE_G), 0, G_SIGMA)
+    for i, (r, c, k) in enumerate(tensors):
+        w = torch.empty((k, r, c), dtype=tdt[spec["w_dtype"]], device="cuda")
+        mm = torch.zeros((k, r, c), dtype=torch.float32, device="cuda")
+        g = torch.empty((k, r, c), dtype=tdt[spec["g_dtype"]], device="cuda")
+        synth.fill_normal_cuda(w, synth.SEED, synth.stream_id(i, synth.ROLE_W), 0, spec["w_sigma"])
+        if spec["m_sigma"] > 0:
+            synth.fill_normal_cuda(mm, synth.SEED, synth.stream_id(i, synth.ROLE_M), 0, spec["m_sigma"])
+        synth.fill_normal_cuda(g, synth.SEED, synth.stream_id(i, synth.ROLE_G), 0, spec["g_sigma"])
         W.append(w); M.append(mm); G.append(g)
     stream = torch.cuda.current_stream()
+    n_mats = int(info.n_matrices)
 
-    def step():
-        nsm.muon_step(plan, W, G, M, LR, MU, True, WD, NS_STEPS, stream)
+    def step(grads=None):
+        nsm.muon_step(plan, W, grads if grads is not None else G, M, LR, MU, True, WD, NS_STEPS, stream)
 
     for _ in range(args.warmup):
         step()
@@ -246,7 +277,7 @@ def run_gpu(args):
     if st != nsm.MUON_OK:
         raise RuntimeError(f"device status {st} after warm-up")
 
-    # ---- timed region: K steps, inputs (1.0 GB) larger than L2 ----
+    # ---- timed region: K steps, inputs larger than L2 ----
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
@@ -269,7 +300,6 @@ def run_gpu(args):
     st, nf = nsm.muon_sync(plan, stream)
     if st != nsm.MUON_OK:
         raise RuntimeError(f"device status {st} after the timed region")
-    n_mats = len(QWEN3_4B_LAYER)
     value = n_mats * world / (ms / 1000.0)
 
     # ---- per-phase times (CUDA events inside the library, one step at a time) ----
@@ -279,51 +309,95 @@ def run_gpu(args):
         s = nsm.muon_get_stats(plan)
         prep.append(s.prep_ms); nsms.append(s.ns_ms + s.apply_ms)
     prep_ms, ns_ms = float(np.median(prep)), float(np.median(nsms))
-    nominal = sum(ns_flops(r, c)[0] for _, r, c in QWEN3_4B_LAYER)
-    algorithmic = sum(ns_flops(r, c)[1] for _, r, c in QWEN3_4B_LAYER)
-    executed = sum(ns_executed_flops(r, c) for _, r, c in QWEN3_4B_LAYER)
-    elems = sum(r * c for _, r, c in QWEN3_4B_LAYER)
-    prep_bytes = 12 * elems
+    nominal = sum(k * ns_flops(r, c)[0] for r, c, k in tensors)
+    algorithmic = sum(k * ns_flops(r, c)[1] for r, c, k in tensors)
+    executed = sum(k * ns_executed_flops(r, c) for r, c, k in tensors)
+    elems = sum(k * r * c for r, c, k in tensors)
+    step_bytes = sum(W[i].numel() * W[i].element_size() + M[i].numel() * 4 + G[i].numel() * G[i].element_size()
+                     for i in range(len(tensors)))
+    prep_bytes = sum(G[i].numel() * (G[i].element_size() + 4 + 4 + 2) for i in range(len(tensors)))
     peaks, peak_kind = load_peaks()
     peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     ns_alg_tflops = algorithmic / (ns_ms * 1e-3) / 1e12
     ns_launches = 3 * NS_STEPS * info.n_buckets
 
     # ---- end to end through the C ABI with host buffers ----
-    hG = [g.cpu().pin_memory() for g in G]
-    hW = [torch.empty_like(w, device="cpu").pin_memory() for w in W]
-    h2d = sum(g.numel() * g.element_size() for g in hG)
-    d2h = sum(w.numel() * w.element_size() for w in hW)
+    # Every step uploads that step's gradients from pinned host memory (on a copy
+    # stream, into one of two device buffers, so step i+1's upload overlaps step i)
+    # and reads back the step's result status word; a second variant reads the
+    # updated weights back every step instead (no overlap possible: the next step
+    # rewrites them).
+    e2e = None
+    if args.workload in ("layer", "single"):
+        hG = [g.cpu().pin_memory() for g in G]
+        dG = [G, [torch.empty_like(g) for g in G]]
+        hstat = [torch.zeros(8, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        copy = torch.cuda.Stream()
+        loaded = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+        for ev in consumed:
+            ev.record(stream)
 
-    def e2e_step():
-        for dg, hg in zip(G, hG):
-            dg.copy_(hg, non_blocking=True)
-        step()
-        for hw, dw in zip(hW, W):
-            hw.copy_(dw, non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            with torch.cuda.stream(copy):
+                copy.wait_event(consumed[b])
+                for dg, hg in zip(dG[b], hG):
+                    dg.copy_(hg, non_blocking=True)
+                loaded[b].record(copy)
+            stream.wait_event(loaded[b])
+            step(dG[b])
+            hstat[b].copy_(ws[:8], non_blocking=True)
+            consumed[b].record(stream)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    k_e2e = max(3, min(args.steps, 50))
-    e0.record(stream)
-    for _ in range(k_e2e):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / k_e2e
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        k_e2e = max(3, min(args.steps, 100))
+        e0.record(stream)
+        for i in range(k_e2e):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / k_e2e
+        hW = [torch.empty_like(w, device="cpu").pin_memory() for w in W]
+
+        def e2e_w_step():
+            for dg, hg in zip(G, hG):
+                dg.copy_(hg, non_blocking=True)
+            step()
+            for hw, dw in zip(hW, W):
+                hw.copy_(dw, non_blocking=True)
+
+        e2e_w_step()
+        torch.cuda.synchronize()
+        k_w = max(3, min(args.steps, 30))
+        e0.record(stream)
+        for _ in range(k_w):
+            e2e_w_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_w_ms = e0.elapsed_time(e1) / k_w
+        if world > 1:
+            t = torch.tensor([e2e_ms, e2e_w_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms, e2e_w_ms = (float(v) for v in t.tolist())
+        h2d = sum(g.numel() * g.element_size() for g in hG)
+        e2e = {"value": n_mats * world / (e2e_ms / 1000.0), "unit": "matrices/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms,
+               "note": "gradients uploaded every step (overlapping the previous step); status word read back",
+               "weights_readback": {"value": n_mats * world / (e2e_w_ms / 1000.0), "unit": "matrices/s",
+                                    "h2d_bytes_per_step": h2d,
+                                    "d2h_bytes_per_step": sum(w.numel() * w.element_size() for w in hW),
+                                    "ms_per_step": e2e_w_ms}}
 
     line = {
         "metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "matrices_per_step": n_mats, "elements_per_step": elems,
+        "config": {"workload": spec["desc"], "matrices_per_step": n_mats, "elements_per_step": elems,
                    "buckets": int(info.n_buckets), "parallelism": f"replicas{world}",
-                   "l2": "inputs 1.0 GB per step, larger than the 129 MB L2"},
+                   "l2": f"inputs {step_bytes / 1e9:.2f} GB per step vs the 129 MB L2"},
         "ns_tflops": {"nominal": nominal / (ms * 1e-3) / 1e12, "algorithmic_in_ns_phase": ns_alg_tflops,
                       "executed_in_ns_phase": executed / (ns_ms * 1e-3) / 1e12,
                       "frac_of_sustained_peak_executed": executed / (ns_ms * 1e-3) / 1e12 / peak_tf,
@@ -339,17 +413,115 @@ def run_gpu(args):
                      "per_launch_ms": ns_ms / ns_launches,
                      "algorithmic_flops_per_launch": algorithmic / ns_launches},
         "clocks": clocks,
-        "e2e": {"value": n_mats * world / (e2e_ms / 1000.0), "unit": "matrices/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * info.n_buckets * (2 + 3 * NS_STEPS),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "layer":
         line["cpu_baseline"] = cpu_baseline_leg()
     if rank == 0:
         print(json.dumps(line), flush=True)
     del ws
     if world > 1:
         dist.destroy_process_group()
+
+
+def host_link_peaks(torch, n_bytes=2 << 30):
+    """Pinned host <-> device copy bandwidth: one direction at a time, then both at once."""
+    h1 = torch.empty(n_bytes, dtype=torch.uint8).pin_memory()
+    h2 = torch.empty(n_bytes, dtype=torch.uint8).pin_memory()
+    d1 = torch.empty(n_bytes, dtype=torch.uint8, device="cuda")
+    d2 = torch.empty(n_bytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t) / reps
+
+    def both():
+        with torch.cuda.stream(s1):
+            d1.copy_(h1, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+
+    out = {"h2d_gbs": n_bytes / timed(lambda: d1.copy_(h1, non_blocking=True)) / 1e9,
+           "d2h_gbs": n_bytes / timed(lambda: h2.copy_(d2, non_blocking=True)) / 1e9,
+           "bidirectional_gbs": 2 * n_bytes / timed(both) / 1e9,
+           "method": "cudaMemcpyAsync of 2 GiB pinned buffers, one direction, then both on two streams"}
+    del h1, h2, d1, d2
+    return out
+
+
+def run_offload(args):
+    """36 Qwen3-4B layers with gradients and fp32 momentum in pinned host memory."""
+    import torch
+    from newton_schulz_muon_gb300.build import build
+    build()
+    import newton_schulz_muon_gb300 as nsm
+    import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    shapes = [(r, c) for _ in range(36) for _, r, c in QWEN3_4B_LAYER]
+    cfg = nsm.muon_config_default(offload=1, max_inflight=2, timing=1)
+    plan = nsm.muon_plan(shapes, bucket_cap_bytes=128 << 20, config=cfg)
+    info = nsm.muon_get_plan_info(plan)
+    ws = nsm.allocate_workspace(plan)
+    hG, hM, hU = [], [], []
+    for i, (r, c) in enumerate(shapes):
+        g = torch.empty((r, c), dtype=torch.bfloat16, device="cuda")
+        mm = torch.empty((r, c), dtype=torch.float32, device="cuda")
+        synth.fill_normal_cuda(g, synth.SEED, synth.stream_id(i, synth.ROLE_G), 0, G_SIGMA)
+        synth.fill_normal_cuda(mm, synth.SEED, synth.stream_id(i, synth.ROLE_M), 0, M_SIGMA)
+        hG.append(torch.empty((r, c), dtype=torch.bfloat16, pin_memory=True).copy_(g))
+        hM.append(torch.empty((r, c), dtype=torch.float32, pin_memory=True).copy_(mm))
+        hU.append(torch.empty((r, c), dtype=torch.float32, pin_memory=True))
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        nsm.muon_offload_step(plan, hG, hM, hU, MU, True, NS_STEPS)
+    times, h2d, d2h = [], [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        a = time.perf_counter()
+        nsm.muon_offload_step(plan, hG, hM, hU, MU, True, NS_STEPS)
+        times.append(time.perf_counter() - a)
+        st = nsm.muon_get_stats(plan)
+        h2d.append(st.h2d_ms); d2h.append(st.d2h_ms)
+    total = time.perf_counter() - t0
+    s_ms = 1000 * float(np.median(times))
+    link = host_link_peaks(torch)
+    hb, db = st.h2d_bytes, st.d2h_bytes
+    algorithmic = sum(ns_flops(r, c)[1] for r, c in shapes)
+    line = {"metric": METRIC, "value": len(shapes) / (s_ms / 1000), "unit": "matrices/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "36 Qwen3-4B layers (3.63B Muon parameters) with G bf16 and fp32 M in pinned "
+                                   "host memory; 128 MiB buckets, three staging slots (upload, compute and "
+                                   "writeback of three buckets overlap); host-blocking step (drained before "
+                                   "return)",
+                       "buckets": int(info.n_buckets), "matrices_per_step": len(shapes)},
+            "host_link": {"h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
+                          "h2d_gbs_avg_over_step": hb / (s_ms * 1e-3) / 1e9,
+                          "d2h_gbs_avg_over_step": db / (s_ms * 1e-3) / 1e9,
+                          "h2d_copy_ms_sum": float(np.median(h2d)), "d2h_copy_ms_sum": float(np.median(d2h)),
+                          "h2d_gbs_while_copying": hb / (float(np.median(h2d)) * 1e-3) / 1e9,
+                          "d2h_gbs_while_copying": db / (float(np.median(d2h)) * 1e-3) / 1e9,
+                          "measured_link": link,
+                          "step_floor_ms": 1000 * max(db / (link["d2h_gbs"] * 1e9), hb / (link["h2d_gbs"] * 1e9),
+                                                      (hb + db) / (link["bidirectional_gbs"] * 1e9)),
+                          "frac_of_link_floor": 1000 * max(db / (link["d2h_gbs"] * 1e9),
+                                                           hb / (link["h2d_gbs"] * 1e9),
+                                                           (hb + db) / (link["bidirectional_gbs"] * 1e9)) / s_ms},
+            "ms_per_step_best": 1000 * float(np.min(times)),
+            "ns_tflops_algorithmic_over_step": algorithmic / (s_ms * 1e-3) / 1e12,
+            "wall_s": total}
+    print(json.dumps(line), flush=True)
+    del ws
 
 
 def main():
@@ -359,11 +531,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["layer", "single", "heads", "experts", "offload"], default="layer",
+                    help="layer (default, the headline) or another measured workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "offload":
+        run_offload(args)
     else:
         run_gpu(args)
 
