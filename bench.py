@@ -73,57 +73,82 @@ def cores_used():
 # ---------------------------------------------------------------------------
 # CPU oracle timing (bench's cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_inputs(names):
+def oracle_sample(spec, n_sample):
+    """Inputs of an evenly spaced sample of the workload's logical matrices, generated on
+    the CPU from the same seeded streams the device fill uses (bit-identical values)."""
     import synth
-    out = {}
-    for i, (name, r, c) in enumerate(QWEN3_4B_LAYER):
-        if name not in names:
-            continue
-        W = synth.tensor(synth.SEED, synth.stream_id(i, synth.ROLE_W), 0, (r, c), W_SIGMA, synth.F32)
-        M = synth.tensor(synth.SEED, synth.stream_id(i, synth.ROLE_M), 0, (r, c), M_SIGMA, synth.F32)
-        G = synth.tensor(synth.SEED, synth.stream_id(i, synth.ROLE_G), 0, (r, c), G_SIGMA, synth.BF16)
-        out[name] = (W.astype(np.float64), M, synth.as_f64(G, synth.BF16))
+    flat = [(i, j, r, c) for i, (r, c, k) in enumerate(spec["tensors"]) for j in range(k)]
+    n = min(n_sample, len(flat))
+    picks = [flat[(q * len(flat)) // n] for q in range(n)]
+    out = []
+    for i, j, r, c in picks:
+        start = j * r * c
+        W = synth.tensor(synth.SEED, synth.stream_id(i, synth.ROLE_W), 0, (r, c), spec["w_sigma"], spec["w_dtype"],
+                         start=start)
+        if spec["m_sigma"] > 0:
+            M = synth.tensor(synth.SEED, synth.stream_id(i, synth.ROLE_M), 0, (r, c), spec["m_sigma"], synth.F32,
+                             start=start)
+        else:
+            M = np.zeros((r, c), dtype=np.float32)
+        G = synth.tensor(synth.SEED, synth.stream_id(i, synth.ROLE_G), 0, (r, c), spec["g_sigma"], spec["g_dtype"],
+                         start=start)
+        out.append((synth.as_f64(W, spec["w_dtype"]), M, synth.as_f64(G, spec["g_dtype"])))
     return out
 
 
-def oracle_step(inputs, names):
+def oracle_step(sample):
     import oracle
-    for name in names:
-        W, M, G = inputs[name]
+    for W, M, G in sample:
         oracle.muon_matrix_step(W, M, G, LR, MU, True, WD, NS_STEPS)
 
 
-def cpu_baseline_leg():
-    names = [n for n, _, _ in QWEN3_4B_LAYER]
-    inputs = oracle_inputs(names)
+# matrices the CPU leg times per workload: the whole layer, or a bounded sample
+CPU_SAMPLE = {"layer": 7, "single": 1, "heads": 64, "experts": 16, "offload": 7}
+
+
+def cpu_baseline_leg(name, min_seconds=3.0):
+    spec = workload_spec("layer" if name == "offload" else name)
+    sample = oracle_sample(spec, CPU_SAMPLE[name])
+    reps, dt = 0, 0.0
     t0 = time.perf_counter()
-    oracle_step(inputs, names)
-    dt = time.perf_counter() - t0
-    return {"value": len(names) / dt, "unit": "matrices/s", "cores": cores_used(), "kind": "oracle",
-            "sample": f"one full step of the 7-matrix layer ({dt:.1f} s, numpy fp64, OpenBLAS threads)"}
+    while reps == 0 or dt < min_seconds:
+        oracle_step(sample)
+        reps += 1
+        dt = time.perf_counter() - t0
+    n = reps * len(sample)
+    what = ("the 7 matrices of one Qwen3-4B layer (the offload step has the same matrices)"
+            if name in ("layer", "offload") else
+            "the workload's one matrix" if len(sample) == 1 else
+            f"{len(sample)} evenly spaced matrices of the workload")
+    return {"value": n / dt, "unit": "matrices/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{what}, {reps} pass(es), {dt:.1f} s; numpy fp64 with OpenBLAS threads"}
 
 
 def run_reference(args):
+    """The oracle, as it stands, on the host cores: the reference arm of this bench."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    names_all = [n for n, _, _ in QWEN3_4B_LAYER]
-    inputs = oracle_inputs(names_all)
-    for _ in range(args.warmup):            # warm-up on the smallest matrix only
-        oracle_step(inputs, ["k_proj"])
+    name = args.workload
+    spec = workload_spec("layer" if name == "offload" else name)
+    sample = oracle_sample(spec, CPU_SAMPLE[name])
+    for _ in range(args.warmup):            # warm-up on the first sampled matrix only
+        oracle_step(sample[:1])
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(inputs, names_all)
+        oracle_step(sample)
     dt = time.perf_counter() - t0
-    value = args.steps * len(names_all) / dt
+    value = args.steps * len(sample) / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "matrices_per_step": 7},
+        "data": "synthetic", "config": {"workload": spec["desc"] if name != "offload" else name,
+                                        "matrices_per_step": len(sample)},
         "cpu_baseline": {"value": value, "unit": "matrices/s", "cores": cores_used(), "kind": "oracle",
-                         "sample": "each timed step is one full oracle step of the 7-matrix layer; "
-                                   "warm-up steps run k_proj only"},
+                         "sample": f"each timed step runs the oracle on {len(sample)} matrices of the workload "
+                                   f"({'all' if name in ('layer', 'offload') else 'evenly spaced'}); "
+                                   "warm-up steps run the first of them only"},
         "e2e": {"value": value, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -195,6 +220,27 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+# DRAM bytes (read + write) per ns_gemm launch on the default workload, averaged
+# over the 15 launches of one step, from one ncu capture (the command and the
+# per-launch table are in profiles/ns_gemm_qwen3_4b_layer.md).  Valid only for the
+# kernel sources it was taken on: the bench reports null once their digest moves.
+NS_GEMM_TRAFFIC = {"bytes_per_launch": 341.0e6, "sources_sha256_16": "b4d5b574b205637c"}
+KERNEL_SOURCES = ("newton_schulz_muon_gb300/csrc/ns_gemm.cu", "newton_schulz_muon_gb300/csrc/device.cuh",
+                  "newton_schulz_muon_gb300/csrc/kernels.h")
+
+
+def ns_gemm_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    root = os.path.dirname(os.path.abspath(__file__))
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != NS_GEMM_TRAFFIC["sources_sha256_16"]:
+        return None
+    return NS_GEMM_TRAFFIC["bytes_per_launch"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -202,6 +248,25 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def launches_per_step(nsm, plan, info):
+    """Kernels one step launches: momentum and norm per bucket, then one
+    small-matrix Newton-Schulz kernel or three GEMMs per iteration."""
+    n = 0
+    for b in range(info.n_buckets):
+        single = nsm.muon_get_bucket_info(plan, b).ns_single_kernel
+        n += 2 + (1 if single else 3 * NS_STEPS)
+    return n
+
+
+def ns_kernel_name(nsm, plan, info):
+    single = [nsm.muon_get_bucket_info(plan, b).ns_single_kernel for b in range(info.n_buckets)]
+    if all(single):
+        return "ns_small_kernel (bf16, every iteration in one launch, with the fused weight update)"
+    if not any(single):
+        return "ns_gemm_kernel (bf16, with the fused weight update)"
+    return "ns_gemm_kernel and ns_small_kernel (bf16, with the fused weight update)"
 
 
 def workload_spec(name):
@@ -319,7 +384,7 @@ def run_gpu(args):
     peaks, peak_kind = load_peaks()
     peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     ns_alg_tflops = algorithmic / (ns_ms * 1e-3) / 1e12
-    ns_launches = 3 * NS_STEPS * info.n_buckets
+    ns_launches = launches_per_step(nsm, plan, info) - 2 * info.n_buckets
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step uploads that step's gradients from pinned host memory (on a copy
@@ -406,19 +471,21 @@ def run_gpu(args):
                      "note": "the weight update runs in the last UPDATE GEMM's epilogue"},
         "elementwise_gbs": {"prep": prep_bytes / (prep_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                             "prep_frac": prep_bytes / (prep_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-        "roofline": {"bound": "tensor", "kernel": "ns_gemm_kernel (bf16, with the fused weight update)",
+        "roofline": {"bound": "tensor", "kernel": ns_kernel_name(nsm, plan, info),
                      "achieved": ns_alg_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": ns_alg_tflops / peak_tf, "traffic": None,
+                     "frac": ns_alg_tflops / peak_tf,
+                     "traffic": ns_gemm_traffic() if args.workload == "layer" else None,
+                     "traffic_unit": "bytes per launch (dram read + write, one ncu capture)",
                      "peak_kind": f"{peak_kind} bf16 sustained (kernel runs inside multi-second loops)",
                      "per_launch_ms": ns_ms / ns_launches,
                      "algorithmic_flops_per_launch": algorithmic / ns_launches},
         "clocks": clocks,
-        "gpu_launches": args.steps * info.n_buckets * (2 + 3 * NS_STEPS),
+        "gpu_launches": args.steps * launches_per_step(nsm, plan, info),
     }
     if e2e is not None:
         line["e2e"] = e2e
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "layer":
-        line["cpu_baseline"] = cpu_baseline_leg()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_leg(args.workload)
     if rank == 0:
         print(json.dumps(line), flush=True)
     del ws
@@ -485,6 +552,8 @@ def run_offload(args):
     for _ in range(args.warmup):
         nsm.muon_offload_step(plan, hG, hM, hU, MU, True, NS_STEPS)
     times, h2d, d2h = [], [], []
+    sampler = ClockSampler(local)
+    sampler.start()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         a = time.perf_counter()
@@ -493,6 +562,7 @@ def run_offload(args):
         st = nsm.muon_get_stats(plan)
         h2d.append(st.h2d_ms); d2h.append(st.d2h_ms)
     total = time.perf_counter() - t0
+    clocks = sampler.stop()
     s_ms = 1000 * float(np.median(times))
     link = host_link_peaks(torch)
     hb, db = st.h2d_bytes, st.d2h_bytes
@@ -519,7 +589,10 @@ def run_offload(args):
                                                            (hb + db) / (link["bidirectional_gbs"] * 1e9)) / s_ms},
             "ms_per_step_best": 1000 * float(np.min(times)),
             "ns_tflops_algorithmic_over_step": algorithmic / (s_ms * 1e-3) / 1e12,
-            "wall_s": total}
+            "wall_s": total, "clocks": clocks,
+            "gpu_launches": args.steps * launches_per_step(nsm, plan, info)}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_leg("offload")
     print(json.dumps(line), flush=True)
     del ws
 

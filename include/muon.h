@@ -63,6 +63,12 @@ typedef int32_t muon_status;
 #define MUON_NS_BF16 0    /* bf16 operands, fp32 accumulation (tcgen05 kind::f16) */
 #define MUON_NS_TF32X3 1  /* fp32 storage, 3xTF32 split products (tcgen05 kind::tf32) */
 
+/* Newton-Schulz kernels */
+#define MUON_NS_KERNEL_AUTO 0 /* buckets whose matrices all have m <= 128 (wide form) run every
+                                 iteration in one kernel with A and B on chip (bf16 only);
+                                 other buckets run three grouped GEMM launches per iteration */
+#define MUON_NS_KERNEL_GEMM 1 /* always the grouped GEMM launches */
+
 /* momentum form (the pages name momentum_update without a formula) */
 #define MUON_MOMENTUM_EMA 0 /* M <- mu M + (1-mu) G;  Nesterov V = (1-mu) G + mu M */
 #define MUON_MOMENTUM_SGD 1 /* M <- mu M + G;         Nesterov V = G + mu M        */
@@ -93,12 +99,13 @@ typedef struct {
                                non-finite values; muon_sync reports the count) */
   int32_t timing;           /* 1: record per-bucket CUDA events for muon_get_stats */
   int32_t offload;          /* 1: reserve host-link staging slots for muon_offload_step */
-  int32_t reserved[4];
+  int32_t ns_kernel;        /* MUON_NS_KERNEL_AUTO or MUON_NS_KERNEL_GEMM */
+  int32_t reserved[3];
 } muon_config;
 
 /* Fills *cfg with (3.4445, -4.7750, 2.0315), eps 1e-7, bf16 NS, EMA momentum,
  * bf16 gradients, fp32 weights, max_inflight 1, skip_nonfinite 1, timing 0,
- * offload 0. */
+ * offload 0, ns_kernel MUON_NS_KERNEL_AUTO. */
 void muon_config_default(muon_config* cfg);
 
 /* Builds the host plan: orients each logical matrix (wide form m x n, m <= n,
@@ -199,12 +206,15 @@ typedef struct {
 muon_status muon_get_plan_info(const muon_plan_t* plan, muon_plan_info* info);
 
 /* Bucket b: number of matrices, wide-form bf16 bytes, same-shape groups in it,
- * and the (m, n) of its first group. */
+ * the (m, n) of its first group, and whether its Newton-Schulz iterations run
+ * in the single small-matrix kernel (1: every group has m <= 128, bf16
+ * arithmetic, ns_kernel AUTO) or as grouped GEMM launches (0). */
 typedef struct {
   int64_t n_matrices;
   int64_t bytes;
   int64_t n_groups;
   int64_t m, n;
+  int64_t ns_single_kernel;
 } muon_bucket_info;
 muon_status muon_get_bucket_info(const muon_plan_t* plan, int64_t b, muon_bucket_info* info);
 

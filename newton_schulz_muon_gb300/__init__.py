@@ -33,6 +33,8 @@ MUON_NS_BF16 = 0
 MUON_NS_TF32X3 = 1
 MUON_MOMENTUM_EMA = 0
 MUON_MOMENTUM_SGD = 1
+MUON_NS_KERNEL_AUTO = 0
+MUON_NS_KERNEL_GEMM = 1
 
 
 class muon_shape(ctypes.Structure):
@@ -43,7 +45,8 @@ class muon_config(ctypes.Structure):
     _fields_ = [("ns_a", c_float), ("ns_b", c_float), ("ns_c", c_float), ("eps", c_float),
                 ("ns_precision", c_int32), ("momentum_form", c_int32), ("grad_dtype", c_int32),
                 ("param_dtype", c_int32), ("max_inflight", c_int32), ("skip_nonfinite", c_int32),
-                ("timing", c_int32), ("offload", c_int32), ("reserved", c_int32 * 4)]
+                ("timing", c_int32), ("offload", c_int32), ("ns_kernel", c_int32),
+                ("reserved", c_int32 * 3)]
 
 
 class muon_plan_info(ctypes.Structure):
@@ -54,7 +57,7 @@ class muon_plan_info(ctypes.Structure):
 
 class muon_bucket_info(ctypes.Structure):
     _fields_ = [("n_matrices", c_int64), ("bytes", c_int64), ("n_groups", c_int64),
-                ("m", c_int64), ("n", c_int64)]
+                ("m", c_int64), ("n", c_int64), ("ns_single_kernel", c_int64)]
 
 
 class muon_stats(ctypes.Structure):

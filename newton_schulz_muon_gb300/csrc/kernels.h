@@ -134,6 +134,33 @@ struct GemmArgs {
   ApplyArgs apply;
 };
 
+// ---------------------------------------------------------------------------
+// Newton-Schulz for wide matrices of at most 128 rows (one CTA per matrix, every
+// iteration in one launch, bf16)
+// ---------------------------------------------------------------------------
+struct SmallGroup {
+  CUtensorMap map_x;     // X (in place across iterations): box {64 columns, 128 rows}
+  void* x;               // bf16 X of matrix 0 of the group in the workspace
+  int64_t ld;            // leading dimension of X (elements)
+  int64_t mstride;       // elements between consecutive matrices
+  int32_t m, n;          // wide form: m <= 128 rows, n columns
+  int32_t count;         // matrices
+  int32_t unit0;         // first launch-wide matrix index of this group
+  int32_t mat_base;      // bucket-local index of matrix 0 (scale, flags, apply)
+  int32_t pad_[3];
+};
+
+struct SmallArgs {
+  SmallGroup g[kMaxGroups];
+  int32_t n_groups;
+  int32_t n_units;       // matrices in the launch
+  int32_t ns_steps;      // quintic iterations (>= 1)
+  float a, b, c;         // X' = a X + (b A + c A A) X, A = X X^T
+  const float* scale;    // per bucket-local matrix: 1 / (||V||_F + eps), folded into iteration 0
+  DeviceStatus* status;
+  ApplyArgs apply;       // the last iteration applies the weight update (or emits U')
+};
+
 // GEMM tile shape (bf16): 128 x 256 outputs per CTA, 64-deep k blocks.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
@@ -149,6 +176,9 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, int cluster, 
 // (a.n_clusters must not exceed it).
 int gemm_max_clusters(bool tf32, int cluster, int num_sms);
 size_t gemm_smem_bytes(bool tf32);
+// All iterations of a bucket whose groups all have m <= 128 (bf16 only).
+cudaError_t launch_ns_small(const SmallArgs& a, int num_sms, cudaStream_t s);
+constexpr int kSmallMaxRows = 128;
 
 // Records `msg` as the calling thread's muon_last_error text and returns `s`.
 int32_t set_error(int32_t s, const char* msg);

@@ -527,10 +527,63 @@ void make_apply_args(const muon_plan_t* p, const Bucket& b, F ptr, int final_buf
   a.flags = at<int32_t>(p, p->off_flags);
 }
 
+// A bucket whose matrices all have at most 128 rows in the wide form.
+bool small_bucket(const Bucket& b) {
+  if (b.groups.empty() || b.groups.size() > (size_t)kMaxGroups) return false;
+  for (const BGroup& g : b.groups)
+    if (g.m > kSmallMaxRows) return false;
+  return true;
+}
+
+bool uses_small_kernel(const muon_config& c, const Bucket& b) {
+  return c.ns_precision == MUON_NS_BF16 && c.ns_kernel == MUON_NS_KERNEL_AUTO && small_bucket(b);
+}
+
+// Every iteration of a small-matrix bucket in one launch (X updated in place in
+// the workspace's first X buffer), the weight update fused into the last one.
+muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st,
+                             const ApplyArgs& fused) {
+  const muon_config& c = p->cfg;
+  SmallArgs sa;
+  std::memset(&sa, 0, sizeof(sa));
+  std::vector<size_t> order(b.groups.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+  // longer matrices first, so the last matrices handed out are the short ones
+  std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) { return b.groups[x].n > b.groups[y].n; });
+  int32_t units = 0;
+  for (size_t gi = 0; gi < order.size(); ++gi) {
+    const BGroup& g = b.groups[order[gi]];
+    SmallGroup& G = sa.g[gi];
+    G.map_x = g.kx[0];
+    G.x = p->ws + p->off_ns + g.off_x[0];
+    G.ld = g.ld_n;
+    G.mstride = g.m * g.ld_n;
+    G.m = (int32_t)g.m;
+    G.n = (int32_t)g.n;
+    G.count = (int32_t)g.count;
+    G.unit0 = units;
+    G.mat_base = (int32_t)g.mat_base;
+    units += (int32_t)g.count;
+  }
+  sa.n_groups = (int32_t)order.size();
+  sa.n_units = units;
+  sa.ns_steps = ns_steps;
+  sa.a = c.ns_a;
+  sa.b = c.ns_b;
+  sa.c = c.ns_c;
+  sa.scale = at<float>(p, p->off_scale);
+  sa.status = at<DeviceStatus>(p, p->off_status);
+  sa.apply = fused;
+  cudaError_t e = launch_ns_small(sa, p->num_sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "small-matrix Newton-Schulz launch");
+  return MUON_OK;
+}
+
 muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st,
                        const ApplyArgs* fused = nullptr) {
   const muon_config& c = p->cfg;
   const bool tf32 = c.ns_precision == MUON_NS_TF32X3;
+  if (fused && ns_steps > 0 && uses_small_kernel(c, b)) return enqueue_ns_small(p, b, ns_steps, st, *fused);
   LaunchShape shapes[3];
   for (int mode = kGram; mode <= kUpdate; ++mode) shapes[mode] = launch_shape(b, mode, tf32);
   for (int it = 0; it < ns_steps; ++it) {
@@ -656,6 +709,7 @@ void muon_config_default(muon_config* cfg) {
   cfg->skip_nonfinite = 1;
   cfg->timing = 0;
   cfg->offload = 0;
+  cfg->ns_kernel = MUON_NS_KERNEL_AUTO;
 }
 
 muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t* groups, int64_t bucket_cap_bytes,
@@ -676,6 +730,8 @@ muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t*
   if (!(c.eps >= 0.f) || !std::isfinite(c.ns_a) || !std::isfinite(c.ns_b) || !std::isfinite(c.ns_c))
     return fail(MUON_ERR_INVALID, "eps must be >= 0 and coefficients finite");
   if (c.max_inflight < 1 || c.max_inflight > 2) return fail(MUON_ERR_INVALID, "max_inflight must be 1 or 2");
+  if (c.ns_kernel != MUON_NS_KERNEL_AUTO && c.ns_kernel != MUON_NS_KERNEL_GEMM)
+    return fail(MUON_ERR_INVALID, "ns_kernel must be AUTO or GEMM");
   muon_plan_t* p = new (std::nothrow) muon_plan_t();
   if (!p) return fail(MUON_ERR_INVALID, "out of host memory");
   p->cfg = c;
@@ -719,6 +775,7 @@ muon_status muon_get_bucket_info(const muon_plan_t* plan, int64_t b, muon_bucket
   info->n_groups = (int64_t)k.groups.size();
   info->m = k.groups[0].m;
   info->n = k.groups[0].n;
+  info->ns_single_kernel = uses_small_kernel(plan->cfg, k) ? 1 : 0;
   return MUON_OK;
 }
 

@@ -38,6 +38,7 @@ def test_config_default(nsm):
     assert c.ns_precision == nsm.MUON_NS_BF16 and c.momentum_form == nsm.MUON_MOMENTUM_EMA
     assert c.grad_dtype == nsm.MUON_DTYPE_BF16 and c.param_dtype == nsm.MUON_DTYPE_F32
     assert c.max_inflight == 1 and c.skip_nonfinite == 1 and c.offload == 0
+    assert c.ns_kernel == nsm.MUON_NS_KERNEL_AUTO
 
 
 QWEN3_4B_LAYER = [(4096, 2560), (1024, 2560), (1024, 2560), (2560, 4096),
@@ -75,6 +76,26 @@ def test_plan_per_head_one_batch(nsm):
     p = nsm.muon_plan(shapes, bucket_cap_bytes=0)
     info = nsm.muon_get_plan_info(p)
     assert info.n_matrices == 1728 and info.n_buckets == 1 and info.n_groups == 1
+
+
+def test_small_matrix_kernel_selection(nsm):
+    # every group m <= 128 in the wide form (tall ones count by their column count)
+    p = nsm.muon_plan([(128, 2560, 48)] * 2 + [(2000, 48), (3, 5)], bucket_cap_bytes=0)
+    assert nsm.muon_get_bucket_info(p, 0).ns_single_kernel == 1
+    # one group with m = 129 sends the bucket to the grouped GEMM launches
+    assert nsm.muon_get_bucket_info(nsm.muon_plan([(128, 512), (129, 512)], bucket_cap_bytes=0),
+                                    0).ns_single_kernel == 0
+    # per bucket: the layer's buckets of k/v (m = 1024) stay on the GEMMs
+    p = nsm.muon_plan([(64, 256, 4), (1024, 2560)], bucket_cap_bytes=200_000)
+    kinds = [nsm.muon_get_bucket_info(p, b).ns_single_kernel for b in range(nsm.muon_get_plan_info(p).n_buckets)]
+    assert kinds[0] == 1 and kinds[-1] == 0
+    # forced off, and not used for 3xTF32
+    cfg = nsm.muon_config_default(ns_kernel=nsm.MUON_NS_KERNEL_GEMM)
+    assert nsm.muon_get_bucket_info(nsm.muon_plan([(128, 2560, 4)], config=cfg), 0).ns_single_kernel == 0
+    cfg = nsm.muon_config_default(ns_precision=nsm.MUON_NS_TF32X3)
+    assert nsm.muon_get_bucket_info(nsm.muon_plan([(128, 2560, 4)], config=cfg), 0).ns_single_kernel == 0
+    with pytest.raises(nsm.MuonError):
+        nsm.muon_plan([(4, 4)], config=nsm.muon_config_default(ns_kernel=2))
 
 
 def test_plan_full_model_offload_layout(nsm):
