@@ -75,6 +75,29 @@ __device__ __forceinline__ void fused_apply_chunk(const ApplyArgs& A, int mat, i
     }
   } else {
     __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(S.w) + base + off0;
+    if (!S.transposed && n == 32 && ((S.cols & 7) == 0) && ((S.stride & 7) == 0)) {
+      // the row's 32 weights are 64 contiguous, 16-byte aligned bytes
+      uint4 raw[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) raw[q] = reinterpret_cast<const uint4*>(w)[q];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t h[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&h[e]);
+          const int j = 8 * q + 2 * e;
+          const float x0 = __low2float(p), x1 = __high2float(p);
+          h[e] = pack_bf16x2(__fmaf_rn(-A.lr, __fmaf_rn(sc, u[j], __fmul_rn(A.wd, x0)), x0),
+                             __fmaf_rn(-A.lr, __fmaf_rn(sc, u[j + 1], __fmul_rn(A.wd, x1)), x1));
+        }
+        raw[q] = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(w)[q] = raw[q];
+      return;
+    }
+    // a tall matrix's column of W is contiguous across the lanes of a warp
     float x[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = j < n ? __bfloat162float(w[j * step]) : 0.f;
