@@ -73,15 +73,17 @@ struct Cfg {
   static constexpr int kBRows = kBN / kCL;                // B rows (or columns) held by one CTA
   static constexpr uint32_t kB = kBRows * 128;            // 32 KB or 16 KB
   static constexpr uint32_t kStage = kParts * (kA + kB);
+  // bf16 epilogue: per epilogue warp a 32 x 32 bf16 chunk, row-major and transposed
+  static constexpr uint32_t kStaging = kTF32 ? 0u : 8u * 2u * 32u * 32u * 2u;
   // as many stages as fit in the 227 KB of dynamic shared memory a CTA may use
   // (1 KB kept for the 1024-byte alignment of the ring, 1 KB for static data)
-  static constexpr int kStages = (int)((232448u - 2048u) / kStage);
+  static constexpr int kStages = (int)((232448u - 2048u - kStaging) / kStage);
   static constexpr uint32_t kTx = kCL * kStage;           // bytes landing per stage on the leader's barrier
   static constexpr int kInstK = kTF32 ? 8 : 16;           // k per MMA instruction
   static constexpr int kChunks = kBRows / kBK;            // MN-major 128-byte column chunks per CTA
   static constexpr uint32_t kChunkBytes = kBK * 128;      // one chunk: kBK k-rows of 128 B
   static constexpr uint32_t kFormat = kTF32 ? 2u : 1u;    // tf32 / bf16 in the instruction descriptor
-  static constexpr size_t kSmem = (size_t)kStages * kStage + 1024;
+  static constexpr size_t kSmem = (size_t)kStages * kStage + kStaging + 1024;
 };
 
 struct TileCoord {
@@ -121,6 +123,11 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmArgs& a, int t, int r
   }
   tc.bi = pi * kCL + rank;
   return tc;
+}
+
+__device__ __forceinline__ uint4 pack8v(const float* v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
 }
 
 // ---------------------------------------------------------------------------
@@ -423,7 +430,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     // split the 256 accumulator columns
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int row_in_tile = quad * 32 + lane;
+    // bf16 epilogue staging of this warp (after the ring): 32 x 32 row-major, then transposed
+    uint4* rowbuf = reinterpret_cast<uint4*>(smem + (size_t)C::kStages * C::kStage + (size_t)(warp - 2) * 4096u);
+    __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(rowbuf) + 2048u);
     const uint32_t tempty_lead[2] = {kCL > 1 ? mapa_shared(&tempty_bar[0], 0) : 0u,
                                      kCL > 1 ? mapa_shared(&tempty_bar[1], 0) : 0u};
     int acc = 0;
@@ -432,7 +441,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       const int t = a.sched_units[si];
       const TileCoord tc = decode_tile<kCL>(a, t, rank);
       const GemmGroup& G = a.g[tc.g];
-      const int64_t r = (int64_t)tc.bi * kBM + row_in_tile;
+      const int64_t row0 = (int64_t)tc.bi * kBM + quad * 32;  // first row of this warp's 32
+      const int64_t r = row0 + lane;
       const int64_t mb = (int64_t)tc.b * G.c_mstride;
       const int64_t ld = G.c_ld;
       // warp-uniform decision: tcgen05.ld below needs every lane of the warp
@@ -451,6 +461,72 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
         float v[32];
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
         const int64_t c0 = (int64_t)tc.bj * kBN + cc * 32;
+        if constexpr (!kTF32) {
+          if (c0 >= G.N) continue;  // the whole chunk lies past the matrix (same for the warp)
+          const bool row_ok = r < G.M;
+          const int64_t valid = G.N - c0;
+          if (mode != kGram) {
+            if (row_ok) Epi<false>::add_d(v, G, mb + r * ld + c0, valid >= 32, valid, alpha, beta);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= alpha;
+          }
+          if (a.fuse_apply) {  // last iteration: update the weights directly, X is not stored
+            if (row_ok) fused_apply_chunk(a.apply, G.mat_base + tc.b, r, c0, valid, v);
+            continue;
+          }
+          // The warp's 32 x 32 chunk goes through shared memory so that the stores
+          // write whole rows: row-major in 16-byte units (unit u of row i at
+          // position u ^ ((i / 2) % 4)), and transposed for the mirror.
+#pragma unroll
+          for (int q = 0; q < 4; ++q) rowbuf[lane * 4 + (q ^ ((lane >> 1) & 3))] = pack8v(v + 8 * q);
+          if (sym) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) tbuf[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+          }
+          __syncwarp();
+          __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(G.c_hi) + mb;
+          const int g = lane & 3;
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            // rows 8 qq .. 8 qq + 7 of the chunk, four lanes per row
+            const int i = 8 * qq + (lane >> 2);
+            const int64_t rr = row0 + i, cg = c0 + 8 * g;
+            const uint4 val = rowbuf[i * 4 + (g ^ ((i >> 1) & 3))];
+            if (rr < G.M && cg < G.N) {
+              if (cg + 8 <= G.N && (!sym || cg >= rr)) {
+                *reinterpret_cast<uint4*>(C + rr * ld + cg) = val;
+              } else {
+                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                  if (cg + h < G.N && (!sym || cg + h >= rr)) C[rr * ld + cg + h] = e[h];
+              }
+            }
+          }
+          if (sym) {
+            // mirror of the strictly upper part: C[c][r] = C[r][c] for c > r;
+            // row c of the mirror is column c of the chunk
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const int ci = 8 * qq + (lane >> 2);
+              const int64_t cr = c0 + ci, rg = row0 + 8 * g;
+              const uint4 val = *reinterpret_cast<const uint4*>(tbuf + ci * 32 + 8 * g);
+              if (cr < G.N) {
+                if (rg + 7 < cr && rg + 8 <= G.M) {
+                  *reinterpret_cast<uint4*>(C + cr * ld + rg) = val;
+                } else {
+                  const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
+#pragma unroll
+                  for (int h = 0; h < 8; ++h)
+                    if (rg + h < G.M && rg + h < cr) C[cr * ld + rg + h] = e[h];
+                }
+              }
+            }
+          }
+          __syncwarp();  // the buffers are rewritten by the next chunk
+          continue;
+        }
         if (r >= G.M || c0 >= G.N) continue;
         const int64_t valid = G.N - c0;  // columns of this chunk inside the matrix
         if (mode != kGram) {
