@@ -73,8 +73,11 @@ struct Cfg {
   static constexpr int kBRows = kBN / kCL;                // B rows (or columns) held by one CTA
   static constexpr uint32_t kB = kBRows * 128;            // 32 KB or 16 KB
   static constexpr uint32_t kStage = kParts * (kA + kB);
-  // bf16 epilogue: per epilogue warp a 32 x 32 bf16 chunk, row-major and transposed
-  static constexpr uint32_t kStaging = kTF32 ? 0u : 8u * 2u * 32u * 32u * 2u;
+  // bf16 epilogue: per epilogue warp 8 KB -- the output chunk (32 x 32 bf16)
+  // row-major and transposed, or the weights of the last UPDATE; and two addend
+  // chunks (the current one and the next, loaded ahead with cp.async)
+  static constexpr uint32_t kWarpStaging = 8192u;
+  static constexpr uint32_t kStaging = kTF32 ? 0u : 8u * kWarpStaging;
   // as many stages as fit in the 227 KB of dynamic shared memory a CTA may use
   // (1 KB kept for the 1024-byte alignment of the ring, 1 KB for static data)
   static constexpr int kStages = (int)((232448u - 2048u - kStaging) / kStage);
@@ -237,6 +240,150 @@ struct Epi<true> {  // 3xTF32: fp32 tf32-high + fp32 low parts
     G.ct_lo[off] = v - h;
   }
 };
+
+// ---------------------------------------------------------------------------
+// bf16 epilogue staging.  A 32 x 32 bf16 chunk is held as 32 rows of four
+// 16-byte units, unit u of row i at position i * 4 + (u ^ ((i / 2) % 4)); the
+// same layout with eight units per row and position i * 8 + (u ^ (i % 8)) holds
+// a 32 x 32 fp32 piece.  Global rows move eight (or four) rows per warp step with
+// 16-byte lanes; a lane reads its own row back (the TMEM row layout).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int unit4(int i, int u) { return i * 4 + (u ^ ((i >> 1) & 3)); }
+__device__ __forceinline__ int unit8(int i, int u) { return i * 8 + (u ^ (i & 7)); }
+
+// Starts copying rows row0 .. +31, columns c0 .. +31 of D into `buf` (cp.async);
+// units outside the matrix are zero, a unit cut by the last column is copied
+// element by element.
+__device__ __forceinline__ void cp_chunk_rows(uint4* buf, const __nv_bfloat16* D, int64_t ld, int64_t M, int64_t N,
+                                              int64_t row0, int64_t c0, int lane) {
+  const int g = lane & 3;
+#pragma unroll 1
+  for (int qq = 0; qq < 4; ++qq) {
+    const int i = 8 * qq + (lane >> 2);
+    const int64_t rr = row0 + i, cg = c0 + 8 * g;
+    uint4* dst = buf + unit4(i, g);
+    if (rr < M && cg + 8 <= N) {
+      cp_async_16(dst, D + rr * ld + cg);
+    } else {
+      uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      if (rr < M && cg < N) {
+        __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&z);
+        for (int h = 0; h < 8; ++h)
+          if (cg + h < N) e[h] = D[rr * ld + cg + h];
+      }
+      *dst = z;
+    }
+  }
+}
+
+// The weights (or U' output) of one matrix for the staged update: a wide matrix
+// whose rows are whole 16-byte units.  ok = false leaves the matrix to
+// fused_apply_chunk (tall matrices, unaligned rows, skipped matrices).
+struct StagedTarget {
+  uint8_t* w;
+  int64_t ld;
+  float sc;
+  bool bf16, ok;
+};
+
+__device__ __forceinline__ StagedTarget staged_target(const ApplyArgs& A, int mat) {
+  int lo = 0, hi = A.n_segs - 1;
+  while (lo < hi) {  // last run with mat0 <= mat
+    const int mid = (lo + hi + 1) >> 1;
+    if (A.seg[mid].mat0 <= mat) lo = mid; else hi = mid - 1;
+  }
+  const ApplySeg& S = A.seg[lo];
+  StagedTarget t;
+  t.bf16 = !A.emit && A.param_dtype != 0;
+  const int64_t per = t.bf16 ? 8 : 4;  // elements per 16-byte unit
+  t.w = reinterpret_cast<uint8_t*>(S.w) + (int64_t)(mat - S.mat0) * S.stride * (t.bf16 ? 2 : 4);
+  t.ld = S.cols;
+  t.sc = S.shape_scale;
+  t.ok = !S.transposed && (S.cols % per) == 0 && (S.stride % per) == 0 &&
+         (reinterpret_cast<uintptr_t>(t.w) & 15u) == 0 && !(!A.emit && A.skip_nonfinite && A.flags[mat]);
+  return t;
+}
+
+// Starts copying the weights of rows row0 .. +31, columns c0 .. +31 into `buf`
+// (nothing when emitting U').
+__device__ __forceinline__ void staged_load(const ApplyArgs& A, const StagedTarget& t, int64_t M, int64_t N,
+                                            int64_t row0, int64_t c0, int lane, uint4* buf) {
+  if (A.emit) return;
+  if (t.bf16) {
+    const int g = lane & 3;
+#pragma unroll 1
+    for (int qq = 0; qq < 4; ++qq) {
+      const int i = 8 * qq + (lane >> 2);
+      const int64_t rr = row0 + i, cg = c0 + 8 * g;
+      if (rr < M && cg < N)
+        cp_async_16(buf + unit4(i, g), reinterpret_cast<const __nv_bfloat16*>(t.w) + rr * t.ld + cg);
+    }
+  } else {
+    const int g = lane & 7;
+#pragma unroll 1
+    for (int qq = 0; qq < 8; ++qq) {
+      const int i = 4 * qq + (lane >> 3);
+      const int64_t rr = row0 + i, cg = c0 + 4 * g;
+      if (rr < M && cg < N)
+        cp_async_16(buf + unit8(i, g), reinterpret_cast<const float*>(t.w) + rr * t.ld + cg);
+    }
+  }
+}
+
+// Lane = row of the chunk, u = its 32 values of U: W <- W - lr (s U + wd W) in
+// the buffer (U' = s U when emitting); then the rows go back to the tensor.
+__device__ __forceinline__ void staged_update_store(const ApplyArgs& A, const StagedTarget& t, int64_t M, int64_t N,
+                                                    int64_t row0, int64_t c0, int lane, const float (&u)[32],
+                                                    uint4* buf) {
+  if (t.bf16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4& cell = buf[unit4(lane, q)];
+      uint32_t h[4] = {cell.x, cell.y, cell.z, cell.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&h[e]);
+        const int j = 8 * q + 2 * e;
+        const float x0 = __low2float(p), x1 = __high2float(p);
+        h[e] = pack_bf16x2(__fmaf_rn(-A.lr, __fmaf_rn(t.sc, u[j], __fmul_rn(A.wd, x0)), x0),
+                           __fmaf_rn(-A.lr, __fmaf_rn(t.sc, u[j + 1], __fmul_rn(A.wd, x1)), x1));
+      }
+      cell = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4* cell = reinterpret_cast<float4*>(buf + unit8(lane, q));
+      float4 w = A.emit ? make_float4(0.f, 0.f, 0.f, 0.f) : *cell;
+      float* wv = reinterpret_cast<float*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        wv[e] = A.emit ? t.sc * u[4 * q + e]
+                       : __fmaf_rn(-A.lr, __fmaf_rn(t.sc, u[4 * q + e], __fmul_rn(A.wd, wv[e])), wv[e]);
+      *cell = w;
+    }
+  }
+  __syncwarp();
+  if (t.bf16) {
+    const int g = lane & 3;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const int i = 8 * qq + (lane >> 2);
+      const int64_t rr = row0 + i, cg = c0 + 8 * g;
+      if (rr < M && cg < N)
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(t.w) + rr * t.ld + cg) = buf[unit4(i, g)];
+    }
+  } else {
+    const int g = lane & 7;
+#pragma unroll
+    for (int qq = 0; qq < 8; ++qq) {
+      const int i = 4 * qq + (lane >> 3);
+      const int64_t rr = row0 + i, cg = c0 + 4 * g;
+      if (rr < M && cg < N)
+        *reinterpret_cast<uint4*>(reinterpret_cast<float*>(t.w) + rr * t.ld + cg) = buf[unit8(i, g)];
+    }
+  }
+}
 
 template <bool kTF32, int kCL>
 __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_constant__ GemmArgs a) {
@@ -430,9 +577,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     // split the 256 accumulator columns
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
-    // bf16 epilogue staging of this warp (after the ring): 32 x 32 row-major, then transposed
-    uint4* rowbuf = reinterpret_cast<uint4*>(smem + (size_t)C::kStages * C::kStage + (size_t)(warp - 2) * 4096u);
-    __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(rowbuf) + 2048u);
+    // bf16 epilogue staging of this warp (after the ring): the output chunk
+    // row-major and transposed (or the last UPDATE's weights), two addend chunks
+    uint8_t* wst = smem + (size_t)C::kStages * C::kStage + (size_t)(warp - 2) * C::kWarpStaging;
+    uint4* rowbuf = reinterpret_cast<uint4*>(wst);
+    __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(wst + 2048u);
+    uint4* dbuf = reinterpret_cast<uint4*>(wst + 4096u);  // addend chunk j at dbuf + (j % 2) * 128
     const uint32_t tempty_lead[2] = {kCL > 1 ? mapa_shared(&tempty_bar[0], 0) : 0u,
                                      kCL > 1 ? mapa_shared(&tempty_bar[1], 0) : 0u};
     int acc = 0;
@@ -445,6 +595,15 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       const int64_t r = row0 + lane;
       const int64_t mb = (int64_t)tc.b * G.c_mstride;
       const int64_t ld = G.c_ld;
+      const __nv_bfloat16* Dm = reinterpret_cast<const __nv_bfloat16*>(G.d_hi) + mb;
+      StagedTarget stg{};
+      if constexpr (!kTF32) {
+        // the first chunk's addend loads while the accumulator is awaited
+        const int64_t c_first = (int64_t)tc.bj * kBN + half * (kBN / 2);
+        if (mode != kGram && c_first < G.N) cp_chunk_rows(dbuf, Dm, ld, G.M, G.N, row0, c_first, lane);
+        cp_async_commit();
+        if (a.fuse_apply) stg = staged_target(a.apply, G.mat_base + tc.b);
+      }
       // warp-uniform decision: tcgen05.ld below needs every lane of the warp
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_p, status);
       if (!__all_sync(0xffffffffu, got)) break;
@@ -458,21 +617,51 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       const bool sym = (mode != kUpdate);
 #pragma unroll 1
       for (int cc = half * (kBN / 64); cc < (half + 1) * (kBN / 64); ++cc) {
-        float v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
         const int64_t c0 = (int64_t)tc.bj * kBN + cc * 32;
         if constexpr (!kTF32) {
-          if (c0 >= G.N) continue;  // the whole chunk lies past the matrix (same for the warp)
+          if (c0 >= G.N) break;  // this and the warp's later chunks lie past the matrix
+          const int k = cc - half * (kBN / 64);
+          // cp.async groups, oldest first: this chunk's addend (committed before),
+          // this chunk's weights, the next chunk's addend
+          const bool staged = a.fuse_apply && stg.ok;
+          if (staged) staged_load(a.apply, stg, G.M, G.N, row0, c0, lane, rowbuf);
+          cp_async_commit();
+          if (mode != kGram && cc + 1 < (half + 1) * (kBN / 64) && c0 + 32 < G.N)
+            cp_chunk_rows(dbuf + ((k + 1) & 1) * 128, Dm, ld, G.M, G.N, row0, c0 + 32, lane);
+          cp_async_commit();
+          float v[32];
+          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
           const bool row_ok = r < G.M;
           const int64_t valid = G.N - c0;
           if (mode != kGram) {
-            if (row_ok) Epi<false>::add_d(v, G, mb + r * ld + c0, valid >= 32, valid, alpha, beta);
+            cp_async_wait<2>();
+            __syncwarp();
+            const uint4* dcur = dbuf + (k & 1) * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 raw = dcur[unit4(lane, q)];
+              const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&w4[h]);
+                v[8 * q + 2 * h] = alpha * v[8 * q + 2 * h] + beta * __low2float(p2);
+                v[8 * q + 2 * h + 1] = alpha * v[8 * q + 2 * h + 1] + beta * __high2float(p2);
+              }
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] *= alpha;
           }
           if (a.fuse_apply) {  // last iteration: update the weights directly, X is not stored
-            if (row_ok) fused_apply_chunk(a.apply, G.mat_base + tc.b, r, c0, valid, v);
+            if (staged) {
+              cp_async_wait<1>();
+              __syncwarp();
+              staged_update_store(a.apply, stg, G.M, G.N, row0, c0, lane, v, rowbuf);
+              __syncwarp();  // rowbuf and this addend buffer are refilled next
+            } else {
+              if (row_ok) fused_apply_chunk(a.apply, G.mat_base + tc.b, r, c0, valid, v);
+              __syncwarp();
+            }
             continue;
           }
           // The warp's 32 x 32 chunk goes through shared memory so that the stores
@@ -527,6 +716,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           __syncwarp();  // the buffers are rewritten by the next chunk
           continue;
         }
+        float v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
         if (r >= G.M || c0 >= G.N) continue;
         const int64_t valid = G.N - c0;  // columns of this chunk inside the matrix
         if (mode != kGram) {
@@ -578,6 +769,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     }
   }
 
+  cp_async_wait<0>();  // no copy into shared memory outlives the CTA
   __syncwarp();
   tc_fence_before();
   __syncthreads();
