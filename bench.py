@@ -224,9 +224,9 @@ class ClockSampler:
 # over the 15 launches of one step, from one ncu capture (the command and the
 # per-launch table are in profiles/ns_gemm_qwen3_4b_layer.md).  Valid only for the
 # kernel sources it was taken on: the bench reports null once their digest moves.
-NS_GEMM_TRAFFIC = {"bytes_per_launch": 341.0e6, "sources_sha256_16": "b4d5b574b205637c"}
+NS_GEMM_TRAFFIC = {"bytes_per_launch": 343.4e6, "sources_sha256_16": "a27d45ceac99919d"}
 KERNEL_SOURCES = ("newton_schulz_muon_gb300/csrc/ns_gemm.cu", "newton_schulz_muon_gb300/csrc/device.cuh",
-                  "newton_schulz_muon_gb300/csrc/kernels.h")
+                  "newton_schulz_muon_gb300/csrc/kernels.h", "newton_schulz_muon_gb300/csrc/epilogue.cuh")
 
 
 def ns_gemm_traffic():
@@ -269,8 +269,9 @@ def ns_kernel_name(nsm, plan, info):
     return "ns_gemm_kernel and ns_small_kernel (bf16, with the fused weight update)"
 
 
-def workload_spec(name):
-    """Tensors (rows, cols, count), dtypes, distributions and bucket cap of a workload."""
+def workload_spec(name, layers=None):
+    """Tensors (rows, cols, count), dtypes, distributions and bucket cap of a workload.
+    `layers` shortens the per-head and expert workloads (for profiling captures)."""
     import synth
     if name == "layer":
         return dict(desc=WORKLOAD, tensors=[(r, c, 1) for _, r, c in QWEN3_4B_LAYER], g_dtype=synth.BF16,
@@ -280,16 +281,18 @@ def workload_spec(name):
                          "lr 0.02, wd 0, 5 NS iterations", tensors=[(256, 512, 1)], g_dtype=synth.F32,
                     g_sigma=1.0, w_dtype=synth.F32, w_sigma=W_SIGMA, m_sigma=0.0, cap=512 << 20)
     if name == "heads":
-        return dict(desc="per-head Muon on fused interleaved QKV [6144, 2560] x 36 layers: 1728 logical 128x2560 "
-                         "matrices in one batch; G bf16 N(0,1e-3), M and W fp32 N(0,0.02)",
-                    tensors=[(128, 2560, 48)] * 36, g_dtype=synth.BF16, g_sigma=G_SIGMA, w_dtype=synth.F32,
+        nl = layers or 36
+        return dict(desc=f"per-head Muon on fused interleaved QKV [6144, 2560] x {nl} layers: {48 * nl} logical "
+                         "128x2560 matrices in one batch; G bf16 N(0,1e-3), M and W fp32 N(0,0.02)",
+                    tensors=[(128, 2560, 48)] * nl, g_dtype=synth.BF16, g_sigma=G_SIGMA, w_dtype=synth.F32,
                     w_sigma=W_SIGMA, m_sigma=M_SIGMA, cap=0)
     if name == "experts":
+        nl = layers or 48
         t = []
-        for _ in range(48):
+        for _ in range(nl):
             t += [(768, 2048, 128), (768, 2048, 128), (2048, 768, 128)]
-        return dict(desc="MoE experts of a 30B-A3B shape: gate/up [128,768,2048], down [128,2048,768] x 48 layers "
-                         "(18432 matrices); G bf16 N(0,1e-3), M zero, W bf16 N(0,0.02); 512 MiB buckets",
+        return dict(desc=f"MoE experts of a 30B-A3B shape: gate/up [128,768,2048], down [128,2048,768] x {nl} "
+                         f"layers ({384 * nl} matrices); G bf16 N(0,1e-3), M zero, W bf16 N(0,0.02); 512 MiB buckets",
                     tensors=t, g_dtype=synth.BF16, g_sigma=G_SIGMA, w_dtype=synth.BF16, w_sigma=W_SIGMA,
                     m_sigma=0.0, cap=512 << 20)
     raise ValueError(name)
@@ -312,7 +315,7 @@ def run_gpu(args):
     import newton_schulz_muon_gb300 as nsm
     import synth
 
-    spec = workload_spec(args.workload)
+    spec = workload_spec(args.workload, args.layers)
     tensors = spec["tensors"]
     shapes = [(r, c, k, 0) for (r, c, k) in tensors]
     cfg = nsm.muon_config_default(timing=1, grad_dtype=spec["g_dtype"], param_dtype=spec["w_dtype"])
@@ -606,6 +609,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["layer", "single", "heads", "experts", "offload"], default="layer",
                     help="layer (default, the headline) or another measured workload")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="heads / experts: fewer layers than the full workload (profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
