@@ -63,6 +63,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values):
+    """Element-wise maximum of per-rank floats over the process group (identity on one
+    rank); CUDA tensors under NCCL, CPU tensors under gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(units_per_rank, world, ms):
+    """Units of all ranks per second, over the slowest rank's time per step."""
+    return units_per_rank * world / (ms / 1000.0)
+
+
 def cores_used():
     try:
         return len(os.sched_getaffinity(0))
@@ -318,7 +336,9 @@ def run_gpu(args):
     spec = workload_spec(args.workload, args.layers)
     tensors = spec["tensors"]
     shapes = [(r, c, k, 0) for (r, c, k) in tensors]
-    cfg = nsm.muon_config_default(timing=1, grad_dtype=spec["g_dtype"], param_dtype=spec["w_dtype"])
+    tf32 = args.ns_precision == "tf32x3"
+    cfg = nsm.muon_config_default(timing=1, grad_dtype=spec["g_dtype"], param_dtype=spec["w_dtype"],
+                                  ns_precision=nsm.MUON_NS_TF32X3 if tf32 else nsm.MUON_NS_BF16)
     plan = nsm.muon_plan(shapes, bucket_cap_bytes=spec["cap"], config=cfg)
     info = nsm.muon_get_plan_info(plan)
     ws = nsm.allocate_workspace(plan)
@@ -361,14 +381,11 @@ def run_gpu(args):
         dist.barrier()
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks([ms])[0]
     st, nf = nsm.muon_sync(plan, stream)
     if st != nsm.MUON_OK:
         raise RuntimeError(f"device status {st} after the timed region")
-    value = n_mats * world / (ms / 1000.0)
+    value = whole_job_rate(n_mats, world, ms)
 
     # ---- per-phase times (CUDA events inside the library, one step at a time) ----
     prep, nsms = [], []
@@ -385,8 +402,12 @@ def run_gpu(args):
                      for i in range(len(tensors)))
     prep_bytes = sum(G[i].numel() * (G[i].element_size() + 4 + 4 + 2) for i in range(len(tensors)))
     peaks, peak_kind = load_peaks()
-    peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    peak_tf = bf16_sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     ns_alg_tflops = algorithmic / (ns_ms * 1e-3) / 1e12
+    if tf32:
+        # 3xTF32: three kind::tf32 products per product; the tf32 peak is the measured
+        # bf16 figure times the nominal tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)
+        peak_tf = peak_tf * 1.1 / 2.25
     ns_launches = launches_per_step(nsm, plan, info) - 2 * info.n_buckets
 
     # ---- end to end through the C ABI with host buffers ----
@@ -446,15 +467,12 @@ def run_gpu(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_w_ms = e0.elapsed_time(e1) / k_w
-        if world > 1:
-            t = torch.tensor([e2e_ms, e2e_w_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms, e2e_w_ms = (float(v) for v in t.tolist())
+        e2e_ms, e2e_w_ms = max_over_ranks([e2e_ms, e2e_w_ms])
         h2d = sum(g.numel() * g.element_size() for g in hG)
-        e2e = {"value": n_mats * world / (e2e_ms / 1000.0), "unit": "matrices/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": whole_job_rate(n_mats, world, e2e_ms), "unit": "matrices/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": 8, "ms_per_step": e2e_ms,
                "note": "gradients uploaded every step (overlapping the previous step); status word read back",
-               "weights_readback": {"value": n_mats * world / (e2e_w_ms / 1000.0), "unit": "matrices/s",
+               "weights_readback": {"value": whole_job_rate(n_mats, world, e2e_w_ms), "unit": "matrices/s",
                                     "h2d_bytes_per_step": h2d,
                                     "d2h_bytes_per_step": sum(w.numel() * w.element_size() for w in hW),
                                     "ms_per_step": e2e_w_ms}}
@@ -462,24 +480,26 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "tf32x3" if tf32 else "bf16", "data": "synthetic",
         "config": {"workload": spec["desc"], "matrices_per_step": n_mats, "elements_per_step": elems,
                    "buckets": int(info.n_buckets), "parallelism": f"replicas{world}",
                    "l2": f"inputs {step_bytes / 1e9:.2f} GB per step vs the 129 MB L2"},
         "ns_tflops": {"nominal": nominal / (ms * 1e-3) / 1e12, "algorithmic_in_ns_phase": ns_alg_tflops,
                       "executed_in_ns_phase": executed / (ns_ms * 1e-3) / 1e12,
-                      "frac_of_sustained_peak_executed": executed / (ns_ms * 1e-3) / 1e12 / peak_tf,
+                      "frac_of_sustained_peak_executed": executed / (ns_ms * 1e-3) / 1e12 / bf16_sustained,
                       "frac_of_burst_peak_executed": executed / (ns_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]},
         "phase_ms": {"prep": prep_ms, "ns_and_apply": ns_ms,
                      "note": "the weight update runs in the last UPDATE GEMM's epilogue"},
         "elementwise_gbs": {"prep": prep_bytes / (prep_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                             "prep_frac": prep_bytes / (prep_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-        "roofline": {"bound": "tensor", "kernel": ns_kernel_name(nsm, plan, info),
-                     "achieved": ns_alg_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": ns_alg_tflops / peak_tf,
-                     "traffic": ns_gemm_traffic() if args.workload == "layer" else None,
+        "roofline": {"bound": "tensor", "kernel": ns_kernel_name(nsm, plan, info) + (", 3xTF32" if tf32 else ""),
+                     "achieved": ns_alg_tflops * (3 if tf32 else 1), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": ns_alg_tflops * (3 if tf32 else 1) / peak_tf,
+                     "traffic": ns_gemm_traffic() if args.workload == "layer" and not tf32 else None,
                      "traffic_unit": "bytes per launch (dram read + write, one ncu capture)",
-                     "peak_kind": f"{peak_kind} bf16 sustained (kernel runs inside multi-second loops)",
+                     "peak_kind": (f"{peak_kind} bf16 sustained x 1.1/2.25 (nominal tf32/bf16); achieved counts "
+                                   "the three tf32 products of each product" if tf32 else
+                                   f"{peak_kind} bf16 sustained (kernel runs inside multi-second loops)"),
                      "per_launch_ms": ns_ms / ns_launches,
                      "algorithmic_flops_per_launch": algorithmic / ns_launches},
         "clocks": clocks,
@@ -609,6 +629,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["layer", "single", "heads", "experts", "offload"], default="layer",
                     help="layer (default, the headline) or another measured workload")
+    ap.add_argument("--ns-precision", choices=["bf16", "tf32x3"], default="bf16",
+                    help="Newton-Schulz arithmetic: bf16 (default) or the 3xTF32 accuracy mode")
     ap.add_argument("--layers", type=int, default=None,
                     help="heads / experts: fewer layers than the full workload (profiling captures)")
     args = ap.parse_args()
