@@ -23,17 +23,23 @@
 // its epilogue instead of storing X.
 //
 // Kernel structure (one persistent CTA per SM, 320 threads):
-//   warp 0:         TMA producer (converged warp, lane 0 issues) over a shared-memory ring of 128-byte-swizzled
-//                   stages: bf16 -- 4 stages of A 128 x 64 + B 256 x 64;
-//                   3xTF32 -- 2 stages of A 128 x 32 and B 256 x 32, each as a
+//   warp 0:         TMA producer (converged warp, lane 0 issues) over a shared-memory
+//                   ring of 128-byte-swizzled stages, as many as fit beside the
+//                   epilogue staging: bf16 -- A 128 x 64 + B (256 / cluster) x 64
+//                   per stage; 3xTF32 -- A 128 x 32 and B x 32, each as a
 //                   tf32-high and a tf32-low fp32 copy
-//   warp 1:         tcgen05.mma issuer (converged warp, lane 0 issues), M=128 N=256 (K=16 bf16 / K=8 tf32), fp32
-//                   accumulators in TMEM, two accumulator buffers (512 columns)
-//                   so the epilogue of one tile overlaps the main loop of the
-//                   next.  3xTF32 issues hi*hi + hi*lo + lo*hi per k step.
+//   warp 1:         tcgen05.mma issuer (converged warp, lane 0 issues), M=128 x
+//                   cluster, N=256 (K=16 bf16 / K=8 tf32), fp32 accumulators in
+//                   TMEM, two accumulator buffers (512 columns) so the epilogue of
+//                   one tile overlaps the main loop of the next.  3xTF32 issues
+//                   hi*hi + hi*lo + lo*hi per k step.
 //   warps 2-9:      epilogue; warp w reads TMEM lanes 32*(w%4)..+31 with
 //                   tcgen05.ld (two warps per lane quadrant, 128 columns each),
-//                   applies alpha/beta, converts and stores.
+//                   adds the alpha/beta term, converts and stores.  bf16: each
+//                   warp owns 8 KB of shared memory through which its 32 x 32
+//                   chunks pass -- the addend arrives there ahead of time by
+//                   cp.async, the output (and the mirror's transpose) leaves in
+//                   whole rows, and the last UPDATE's weights go the same way.
 // Tiles of all same-shape groups of a micro-bucket (and of all its matrices) are
 // numbered in one space; a host-computed longest-processing-time schedule gives
 // each cluster its list of tiles.
@@ -140,51 +146,7 @@ template <bool kTF32>
 struct Epi;
 
 template <>
-struct Epi<false> {  // bf16 storage
-  static __device__ __forceinline__ void add_d(float (&v)[32], const GemmGroup& G, int64_t off, bool full,
-                                               int64_t valid, float alpha, float beta) {
-    const __nv_bfloat16* drow = reinterpret_cast<const __nv_bfloat16*>(G.d_hi) + off;
-    if (full) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(drow + 8 * q);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w4[h]);
-          v[8 * q + 2 * h] = alpha * v[8 * q + 2 * h] + beta * __low2float(p);
-          v[8 * q + 2 * h + 1] = alpha * v[8 * q + 2 * h + 1] + beta * __high2float(p);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = alpha * v[j] + (j < valid ? beta * __bfloat162float(drow[j]) : 0.f);
-    }
-  }
-  // store columns [8q, 8q+8) of the chunk when `all8`, else the masked ones
-  static __device__ __forceinline__ void store8(const GemmGroup& G, int64_t off, const float* v, bool all8,
-                                                unsigned mask) {
-    __nv_bfloat16* c = reinterpret_cast<__nv_bfloat16*>(G.c_hi) + off;
-    if (all8) {
-      uint4 raw;
-      raw.x = pack_bf16x2(v[0], v[1]);
-      raw.y = pack_bf16x2(v[2], v[3]);
-      raw.z = pack_bf16x2(v[4], v[5]);
-      raw.w = pack_bf16x2(v[6], v[7]);
-      *reinterpret_cast<uint4*>(c) = raw;
-    } else {
-#pragma unroll
-      for (int h = 0; h < 8; ++h)
-        if (mask & (1u << h)) c[h] = __float2bfloat16_rn(v[h]);
-    }
-  }
-  static __device__ __forceinline__ void store1(const GemmGroup& G, int64_t off, float v) {
-    reinterpret_cast<__nv_bfloat16*>(G.c_hi)[off] = __float2bfloat16_rn(v);
-  }
-};
-
-template <>
-struct Epi<true> {  // 3xTF32: fp32 tf32-high + fp32 low parts
+struct Epi<true> {  // 3xTF32: fp32 tf32-high + fp32 low parts (the bf16 epilogue is staged, below)
   static __device__ __forceinline__ void add_d(float (&v)[32], const GemmGroup& G, int64_t off, bool full,
                                                int64_t valid, float alpha, float beta) {
     const float* dh = reinterpret_cast<const float*>(G.d_hi) + off;
@@ -715,45 +677,44 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           }
           __syncwarp();  // the buffers are rewritten by the next chunk
           continue;
-        }
-        float v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
-        if (r >= G.M || c0 >= G.N) continue;
-        const int64_t valid = G.N - c0;  // columns of this chunk inside the matrix
-        if (mode != kGram) {
-          Epi<kTF32>::add_d(v, G, mb + r * ld + c0, valid >= 32, valid, alpha, beta);
         } else {
+          float v[32];
+          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
+          if (r >= G.M || c0 >= G.N) continue;
+          const int64_t valid = G.N - c0;  // columns of this chunk inside the matrix
+          if (mode != kGram) {
+            Epi<true>::add_d(v, G, mb + r * ld + c0, valid >= 32, valid, alpha, beta);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= alpha;
-        }
-        if (a.fuse_apply) {  // last iteration: update the weights directly, X is not stored
-          fused_apply_chunk(a.apply, G.mat_base + tc.b, r, c0, valid, v);
-          continue;
-        }
-        // direct store of row r (upper part only in the symmetric modes)
+            for (int j = 0; j < 32; ++j) v[j] *= alpha;
+          }
+          if (a.fuse_apply) {  // last iteration: update the weights directly, X is not stored
+            fused_apply_chunk(a.apply, G.mat_base + tc.b, r, c0, valid, v);
+            continue;
+          }
+          // direct store of row r (upper part only in the symmetric modes)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t cq = c0 + 8 * q;
-          unsigned mask = 0;
+          for (int q = 0; q < 4; ++q) {
+            const int64_t cq = c0 + 8 * q;
+            unsigned mask = 0;
 #pragma unroll
-          for (int h = 0; h < 8; ++h)
-            if (cq + h < G.N && (!sym || cq + h >= r)) mask |= 1u << h;
-          Epi<kTF32>::store8(G, mb + r * ld + cq, v + 8 * q, mask == 0xFFu, mask);
-        }
-        if constexpr (kTF32) {
+            for (int h = 0; h < 8; ++h)
+              if (cq + h < G.N && (!sym || cq + h >= r)) mask |= 1u << h;
+            Epi<true>::store8(G, mb + r * ld + cq, v + 8 * q, mask == 0xFFu, mask);
+          }
           if (mode == kUpdate) {  // X'^T[c][r] for the next UPDATE's K-major B operand
             const int64_t mbt = (int64_t)tc.b * G.ct_mstride;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (c0 + j < G.N) Epi<true>::store1t(G, mbt + (c0 + j) * G.ct_ld + r, v[j]);
           }
-        }
-        // mirror of the strictly upper part: C[c][r] = C[r][c]
-        if (sym) {
+          // mirror of the strictly upper part: C[c][r] = C[r][c]
+          if (sym) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t c = c0 + j;
-            if (c > r && c < G.N) Epi<kTF32>::store1(G, mb + c * ld + r, v[j]);
+            for (int j = 0; j < 32; ++j) {
+              const int64_t c = c0 + j;
+              if (c > r && c < G.N) Epi<true>::store1(G, mb + c * ld + r, v[j]);
+            }
           }
         }
       }
