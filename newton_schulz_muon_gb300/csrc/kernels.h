@@ -98,6 +98,8 @@ struct GemmGroup {
   CUtensorMap map_b;     // operand B (K-major box {64, 128} x2, or bf16 UPDATE: MN-major box {64, 64} x4)
   CUtensorMap map_a_lo;  // 3xTF32: low parts (unused in bf16 mode)
   CUtensorMap map_b_lo;
+  CUtensorMap map_c;     // bf16 epilogue: output C, box {32, 32}, 64-byte swizzle (TMA stores)
+  CUtensorMap map_d;     // bf16 epilogue: addend D, same box (TMA loads)
   void* c_hi;            // output (bf16 or tf32-hi fp32)
   float* c_lo;           // output tf32-lo part
   const void* d_hi;      // epilogue addend (POLY: A, UPDATE: X)

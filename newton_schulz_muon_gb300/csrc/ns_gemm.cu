@@ -37,9 +37,10 @@
 //                   tcgen05.ld (two warps per lane quadrant, 128 columns each),
 //                   adds the alpha/beta term, converts and stores.  bf16: each
 //                   warp owns 8 KB of shared memory through which its 32 x 32
-//                   chunks pass -- the addend arrives there ahead of time by
-//                   cp.async, the output (and the mirror's transpose) leaves in
-//                   whole rows, and the last UPDATE's weights go the same way.
+//                   chunks pass as TMA boxes -- the addend is requested one
+//                   chunk ahead (across tiles) into two slots with their own
+//                   mbarriers, the output and the mirror's transpose leave as
+//                   TMA stores, and the last UPDATE's weights move by cp.async.
 // Tiles of all same-shape groups of a micro-bucket (and of all its matrices) are
 // numbered in one space; a host-computed longest-processing-time schedule gives
 // each cluster its list of tiles.
@@ -80,8 +81,8 @@ struct Cfg {
   static constexpr uint32_t kB = kBRows * 128;            // 32 KB or 16 KB
   static constexpr uint32_t kStage = kParts * (kA + kB);
   // bf16 epilogue: per epilogue warp 8 KB -- the output chunk (32 x 32 bf16)
-  // row-major and transposed, or the weights of the last UPDATE; and two addend
-  // chunks (the current one and the next, loaded ahead with cp.async)
+  // and its transpose, or the weights of the last UPDATE; and two addend chunks
+  // (the current one and the next, TMA boxes)
   static constexpr uint32_t kWarpStaging = 8192u;
   static constexpr uint32_t kStaging = kTF32 ? 0u : 8u * kWarpStaging;
   // as many stages as fit in the 227 KB of dynamic shared memory a CTA may use
@@ -205,38 +206,15 @@ struct Epi<true> {  // 3xTF32: fp32 tf32-high + fp32 low parts (the bf16 epilogu
 
 // ---------------------------------------------------------------------------
 // bf16 epilogue staging.  A 32 x 32 bf16 chunk is held as 32 rows of four
-// 16-byte units, unit u of row i at position i * 4 + (u ^ ((i / 2) % 4)); the
-// same layout with eight units per row and position i * 8 + (u ^ (i % 8)) holds
-// a 32 x 32 fp32 piece.  Global rows move eight (or four) rows per warp step with
-// 16-byte lanes; a lane reads its own row back (the TMEM row layout).
+// 16-byte units, unit u of row i at position i * 4 + (u ^ ((i / 2) % 4)): the
+// order in which a TMA box of 64-byte rows lands with the 64-byte swizzle (the
+// buffers are 2 KB aligned), so such chunks move as TMA boxes.  The same idea
+// with eight units per row, position i * 8 + (u ^ (i % 8)), holds a 32 x 32 fp32
+// piece of weights, whose global rows move eight (or four) rows per warp step
+// with 16-byte lanes.  A lane reads its own row back (the TMEM row layout).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int unit4(int i, int u) { return i * 4 + (u ^ ((i >> 1) & 3)); }
 __device__ __forceinline__ int unit8(int i, int u) { return i * 8 + (u ^ (i & 7)); }
-
-// Starts copying rows row0 .. +31, columns c0 .. +31 of D into `buf` (cp.async);
-// units outside the matrix are zero, a unit cut by the last column is copied
-// element by element.
-__device__ __forceinline__ void cp_chunk_rows(uint4* buf, const __nv_bfloat16* D, int64_t ld, int64_t M, int64_t N,
-                                              int64_t row0, int64_t c0, int lane) {
-  const int g = lane & 3;
-#pragma unroll 1
-  for (int qq = 0; qq < 4; ++qq) {
-    const int i = 8 * qq + (lane >> 2);
-    const int64_t rr = row0 + i, cg = c0 + 8 * g;
-    uint4* dst = buf + unit4(i, g);
-    if (rr < M && cg + 8 <= N) {
-      cp_async_16(dst, D + rr * ld + cg);
-    } else {
-      uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      if (rr < M && cg < N) {
-        __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&z);
-        for (int h = 0; h < 8; ++h)
-          if (cg + h < N) e[h] = D[rr * ld + cg + h];
-      }
-      *dst = z;
-    }
-  }
-}
 
 // The weights (or U' output) of one matrix for the staged update: a wide matrix
 // whose rows are whole 16-byte units.  ok = false leaves the matrix to
@@ -359,6 +337,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t addend_bar[16];  // two per epilogue warp
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -382,6 +361,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       mbar_init(&tempty_bar[i], kCL == 1 ? 256 : 8 * kCL);
     }
     mbar_init(&drain_bar, 1);
+    for (int i = 0; i < 16; ++i) mbar_init(&addend_bar[i], 1);
     abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -536,20 +516,37 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
   } else {
     // ---------------- epilogue (warps 2..9 of both CTAs) ----------------
     // warp w reads TMEM lanes 32*(w%4)..+31; the two warps of a lane quadrant
-    // split the 256 accumulator columns
+    // split the 256 accumulator columns into 32-column chunks
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
-    // bf16 epilogue staging of this warp (after the ring): the output chunk
-    // row-major and transposed (or the last UPDATE's weights), two addend chunks
-    uint8_t* wst = smem + (size_t)C::kStages * C::kStage + (size_t)(warp - 2) * C::kWarpStaging;
+    const int ew = warp - 2;
+    // bf16 staging of this warp (after the ring), every buffer one 32 x 32 box in
+    // the 64-byte swizzle: the output chunk and its transpose (or the last
+    // UPDATE's weights), and two addend slots filled by TMA
+    uint8_t* wst = smem + (size_t)C::kStages * C::kStage + (size_t)ew * C::kWarpStaging;
     uint4* rowbuf = reinterpret_cast<uint4*>(wst);
     __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(wst + 2048u);
-    uint4* dbuf = reinterpret_cast<uint4*>(wst + 4096u);  // addend chunk j at dbuf + (j % 2) * 128
+    uint4* dbuf = reinterpret_cast<uint4*>(wst + 4096u);  // addend slot s at dbuf + s * 128
+    uint64_t* dbar = &addend_bar[2 * ew];
     const uint32_t tempty_lead[2] = {kCL > 1 ? mapa_shared(&tempty_bar[0], 0) : 0u,
                                      kCL > 1 ? mapa_shared(&tempty_bar[1], 0) : 0u};
+    const int s_end = a.sched_off[cluster_id + 1];
+    // addend chunks are requested in the order they are used, one ahead, across
+    // tiles: request q lands in slot q % 2 and completes phase (q / 2) % 2
+    const bool has_d = !kTF32 && mode != kGram;
+    int d_req = 0, d_use = 0;
+    auto d_request = [&](const GemmGroup& Gx, int b, int64_t r0, int64_t c) {
+      const int s = d_req & 1;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&dbar[s], 2048u);
+        tma_load_3d(dbuf + s * 128, &Gx.map_d, &dbar[s], (int)c, (int)r0, b);
+      }
+      ++d_req;
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int si = a.sched_off[cluster_id]; si < a.sched_off[cluster_id + 1]; ++si) {
+    bool failed = false;
+    for (int si = a.sched_off[cluster_id]; si < s_end && !failed; ++si) {
       const int t = a.sched_units[si];
       const TileCoord tc = decode_tile<kCL>(a, t, rank);
       const GemmGroup& G = a.g[tc.g];
@@ -557,13 +554,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       const int64_t r = row0 + lane;
       const int64_t mb = (int64_t)tc.b * G.c_mstride;
       const int64_t ld = G.c_ld;
-      const __nv_bfloat16* Dm = reinterpret_cast<const __nv_bfloat16*>(G.d_hi) + mb;
+      const int64_t c_first = (int64_t)tc.bj * kBN + half * (kBN / 2);
+      // this warp's chunks that start inside the matrix
+      const int nch = c_first < G.N ? (int)min((int64_t)(kBN / 64), (G.N - c_first + 31) / 32) : 0;
       StagedTarget stg{};
       if constexpr (!kTF32) {
-        // the first chunk's addend loads while the accumulator is awaited
-        const int64_t c_first = (int64_t)tc.bj * kBN + half * (kBN / 2);
-        if (mode != kGram && c_first < G.N) cp_chunk_rows(dbuf, Dm, ld, G.M, G.N, row0, c_first, lane);
-        cp_async_commit();
+        // the first addend chunk loads while the accumulator is awaited, unless
+        // the previous tile requested it already
+        if (has_d && nch > 0 && d_req == d_use) d_request(G, tc.b, row0, c_first);
         if (a.fuse_apply) stg = staged_target(a.apply, G.mat_base + tc.b);
       }
       // warp-uniform decision: tcgen05.ld below needs every lane of the warp
@@ -578,27 +576,34 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       }
       const bool sym = (mode != kUpdate);
 #pragma unroll 1
-      for (int cc = half * (kBN / 64); cc < (half + 1) * (kBN / 64); ++cc) {
+      for (int k = 0; k < (kTF32 ? kBN / 64 : nch); ++k) {
+        const int cc = half * (kBN / 64) + k;
         const int64_t c0 = (int64_t)tc.bj * kBN + cc * 32;
         if constexpr (!kTF32) {
-          if (c0 >= G.N) break;  // this and the warp's later chunks lie past the matrix
-          const int k = cc - half * (kBN / 64);
-          // cp.async groups, oldest first: this chunk's addend (committed before),
-          // this chunk's weights, the next chunk's addend
           const bool staged = a.fuse_apply && stg.ok;
           if (staged) staged_load(a.apply, stg, G.M, G.N, row0, c0, lane, rowbuf);
           cp_async_commit();
-          if (mode != kGram && cc + 1 < (half + 1) * (kBN / 64) && c0 + 32 < G.N)
-            cp_chunk_rows(dbuf + ((k + 1) & 1) * 128, Dm, ld, G.M, G.N, row0, c0 + 32, lane);
-          cp_async_commit();
+          // the next addend chunk: this tile's next, else the next tile's first
+          if (has_d && d_req == d_use + 1) {
+            if (k + 1 < nch) {
+              d_request(G, tc.b, row0, c0 + 32);
+            } else if (si + 1 < s_end) {
+              const TileCoord tn = decode_tile<kCL>(a, a.sched_units[si + 1], rank);
+              const GemmGroup& Gn = a.g[tn.g];
+              const int64_t cn = (int64_t)tn.bj * kBN + half * (kBN / 2);
+              if (cn < Gn.N) d_request(Gn, tn.b, (int64_t)tn.bi * kBM + quad * 32, cn);
+            }
+          }
           float v[32];
           tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
           const bool row_ok = r < G.M;
           const int64_t valid = G.N - c0;
-          if (mode != kGram) {
-            cp_async_wait<2>();
-            __syncwarp();
-            const uint4* dcur = dbuf + (k & 1) * 128;
+          if (has_d) {
+            const int s = d_use & 1;
+            const bool landed = mbar_wait(&dbar[s], (uint32_t)(d_use >> 1) & 1u, abort_p, status);
+            if (!__all_sync(0xffffffffu, landed)) { failed = true; break; }
+            ++d_use;
+            const uint4* dcur = dbuf + s * 128;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint4 raw = dcur[unit4(lane, q)];
@@ -616,63 +621,64 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           }
           if (a.fuse_apply) {  // last iteration: update the weights directly, X is not stored
             if (staged) {
-              cp_async_wait<1>();
+              cp_async_wait<0>();
               __syncwarp();
               staged_update_store(a.apply, stg, G.M, G.N, row0, c0, lane, v, rowbuf);
-              __syncwarp();  // rowbuf and this addend buffer are refilled next
-            } else {
-              if (row_ok) fused_apply_chunk(a.apply, G.mat_base + tc.b, r, c0, valid, v);
-              __syncwarp();
+            } else if (row_ok) {
+              fused_apply_chunk(a.apply, G.mat_base + tc.b, r, c0, valid, v);
             }
+            __syncwarp();  // the addend slot and rowbuf are refilled next
             continue;
           }
-          // The warp's 32 x 32 chunk goes through shared memory so that the stores
-          // write whole rows: row-major in 16-byte units (unit u of row i at
-          // position u ^ ((i / 2) % 4)), and transposed for the mirror.
-#pragma unroll
-          for (int q = 0; q < 4; ++q) rowbuf[lane * 4 + (q ^ ((lane >> 1) & 3))] = pack8v(v + 8 * q);
-          if (sym) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) tbuf[j * 32 + lane] = __float2bfloat16_rn(v[j]);
+          // In the symmetric modes only the upper triangle is stored, and its
+          // mirror: a chunk below the diagonal stores nothing, one above it goes
+          // out as two TMA boxes (the chunk and its transpose), one on the
+          // diagonal element by element.
+          if (row0 >= G.M || (sym && c0 + 32 <= row0)) {
+            __syncwarp();
+            continue;
           }
+          if (lane == 0) bulk_wait_group_read<0>();  // the last boxes have left the staging
           __syncwarp();
-          __nv_bfloat16* C = reinterpret_cast<__nv_bfloat16*>(G.c_hi) + mb;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) rowbuf[unit4(lane, q)] = pack8v(v + 8 * q);
+          if (sym) {
+            // row j of the transpose is column j of the chunk; lane = its element
+            const int e = lane & 7, u = lane >> 3;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) tbuf[j * 32 + ((u ^ ((j >> 1) & 3)) << 3) + e] = __float2bfloat16_rn(v[j]);
+          }
+          if (!sym || c0 >= row0 + 32) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&G.map_c, rowbuf, (int)c0, (int)row0, tc.b);
+              if (sym) tma_store_3d(&G.map_c, tbuf, (int)row0, (int)c0, tc.b);
+              bulk_commit_group();
+            }
+            __syncwarp();
+            continue;
+          }
+          // diagonal chunk (c0 == row0): the upper part, and its mirror C[c][r] for c > r
+          __syncwarp();
+          __nv_bfloat16* Cm = reinterpret_cast<__nv_bfloat16*>(G.c_hi) + mb;
+          const uint4* tb4 = reinterpret_cast<const uint4*>(tbuf);
           const int g = lane & 3;
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
-            // rows 8 qq .. 8 qq + 7 of the chunk, four lanes per row
             const int i = 8 * qq + (lane >> 2);
             const int64_t rr = row0 + i, cg = c0 + 8 * g;
-            const uint4 val = rowbuf[i * 4 + (g ^ ((i >> 1) & 3))];
-            if (rr < G.M && cg < G.N) {
-              if (cg + 8 <= G.N && (!sym || cg >= rr)) {
-                *reinterpret_cast<uint4*>(C + rr * ld + cg) = val;
-              } else {
-                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
+            const uint4 val = rowbuf[unit4(i, g)];
+            const uint4 tv = tb4[unit4(i, g)];
+            const __nv_bfloat16* ev = reinterpret_cast<const __nv_bfloat16*>(&val);
+            const __nv_bfloat16* et = reinterpret_cast<const __nv_bfloat16*>(&tv);
+            // direct: row rr, columns cg .. cg + 7 with column >= row
+            // mirror: row c0 + i, columns row0 + 8g .. +7 with column < row
 #pragma unroll
-                for (int h = 0; h < 8; ++h)
-                  if (cg + h < G.N && (!sym || cg + h >= rr)) C[rr * ld + cg + h] = e[h];
-              }
-            }
-          }
-          if (sym) {
-            // mirror of the strictly upper part: C[c][r] = C[r][c] for c > r;
-            // row c of the mirror is column c of the chunk
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const int ci = 8 * qq + (lane >> 2);
-              const int64_t cr = c0 + ci, rg = row0 + 8 * g;
-              const uint4 val = *reinterpret_cast<const uint4*>(tbuf + ci * 32 + 8 * g);
-              if (cr < G.N) {
-                if (rg + 7 < cr && rg + 8 <= G.M) {
-                  *reinterpret_cast<uint4*>(C + cr * ld + rg) = val;
-                } else {
-                  const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
-#pragma unroll
-                  for (int h = 0; h < 8; ++h)
-                    if (rg + h < G.M && rg + h < cr) C[cr * ld + rg + h] = e[h];
-                }
-              }
+            for (int h = 0; h < 8; ++h) {
+              if (rr < G.M && cg + h < G.N && cg + h >= rr) Cm[rr * ld + cg + h] = ev[h];
+              const int64_t mr = c0 + i, mc = row0 + 8 * g + h;
+              if (mr < G.N && mc < G.M && mc < mr) Cm[mr * ld + mc] = et[h];
             }
           }
           __syncwarp();  // the buffers are rewritten by the next chunk
@@ -718,6 +724,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           }
         }
       }
+      if (failed) break;
       tc_fence_before();
       if constexpr (kCL == 1) {
         mbar_arrive(&tempty_bar[acc]);
@@ -727,6 +734,16 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+    }
+    if constexpr (!kTF32) {
+      if (lane == 0) {
+        // addend boxes still in flight land before the CTA exits (bounded), and
+        // the output boxes are written
+        for (int q = d_use; q < d_req; ++q)
+          (void)mbar_wait(&dbar[q & 1], (uint32_t)(q >> 1) & 1u, nullptr, nullptr, 100000000ull);
+        bulk_wait_group<0>();
+      }
+      __syncwarp();
     }
   }
 

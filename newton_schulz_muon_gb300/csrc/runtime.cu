@@ -90,6 +90,7 @@ struct BGroup {
   CUtensorMap kx[2], mx[2], ka, kb;
   CUtensorMap kx_lo[2], mx_lo[2], ka_lo, kb_lo;
   CUtensorMap kxt[2], kxt_lo[2];
+  CUtensorMap ex[2], ea, eb;  // bf16 GEMM epilogue boxes of 32 x 32 (64-byte swizzle)
 };
 
 struct Bucket {
@@ -172,7 +173,8 @@ EncodeTiledFn get_encode_fn() {
 
 // [count][rows][ld] array of `esize`-byte elements; logical (cols, rows, count).
 bool encode_map(CUtensorMap* map, void* base, size_t esize, int64_t cols, int64_t rows, int64_t count,
-                int64_t ld, uint32_t box_x, uint32_t box_y) {
+                int64_t ld, uint32_t box_x, uint32_t box_y,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)count};
@@ -181,7 +183,7 @@ bool encode_map(CUtensorMap* map, void* base, size_t esize, int64_t cols, int64_
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   CUresult r = fn(map, dt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -618,12 +620,14 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
         if (mode == kGram) {
           G.map_a = g.kx[cur]; G.map_b = g.kx[cur];
           if (tf32) { G.map_a_lo = g.kx_lo[cur]; G.map_b_lo = g.kx_lo[cur]; }
+          if (!tf32) G.map_c = g.ea;
           G.c_hi = ns + g.off_a; G.c_lo = lo(g.off_a_lo);
           G.d_hi = nullptr; G.d_lo = nullptr;
           G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
         } else if (mode == kPoly) {
           G.map_a = g.ka; G.map_b = g.ka;
           if (tf32) { G.map_a_lo = g.ka_lo; G.map_b_lo = g.ka_lo; }
+          if (!tf32) { G.map_c = g.eb; G.map_d = g.ea; }
           G.c_hi = ns + g.off_b; G.c_lo = lo(g.off_b_lo);
           G.d_hi = ns + g.off_a; G.d_lo = lo(g.off_a_lo);
           G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
@@ -636,6 +640,7 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
             G.ct_hi = ns + g.off_xt[nxt]; G.ct_lo = lo(g.off_xt_lo[nxt]);
             G.ct_ld = g.ld_t; G.ct_mstride = g.n * g.ld_t;
           }
+          if (!tf32) { G.map_c = g.ex[nxt]; G.map_d = g.ex[cur]; }
           G.c_hi = ns + g.off_x[nxt]; G.c_lo = lo(g.off_x_lo[nxt]);
           G.d_hi = ns + g.off_x[cur]; G.d_lo = lo(g.off_x_lo[cur]);
           G.c_ld = g.ld_n; G.c_mstride = g.m * g.ld_n;
@@ -818,6 +823,14 @@ muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes
       }
       ok &= encode_map(&g.ka, ns + g.off_a, es, g.m, g.m, g.count, g.ld_m, kbox, 128);
       ok &= encode_map(&g.kb, ns + g.off_b, es, g.m, g.m, g.count, g.ld_m, kbox, 128);
+      if (!tf32) {
+        // the epilogue's 32 x 32 chunks: 64-byte rows, swizzled like its staging
+        const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
+        for (int i = 0; i < 2; ++i)
+          ok &= encode_map(&g.ex[i], ns + g.off_x[i], es, g.n, g.m, g.count, g.ld_n, 32, 32, sw);
+        ok &= encode_map(&g.ea, ns + g.off_a, es, g.m, g.m, g.count, g.ld_m, 32, 32, sw);
+        ok &= encode_map(&g.eb, ns + g.off_b, es, g.m, g.m, g.count, g.ld_m, 32, 32, sw);
+      }
       if (tf32) {
         for (int i = 0; i < 2; ++i) {
           ok &= encode_map(&g.kx_lo[i], ns + g.off_x_lo[i], es, g.n, g.m, g.count, g.ld_n, kbox, 128);
