@@ -123,7 +123,8 @@ struct GemmArgs {
   int32_t total_tiles;
   int32_t mode;
   int32_t use_scale;      // first iteration: fold 1/(||V||+eps) into the epilogue
-  float alpha, beta;      // GRAM: 1, -; POLY: c, b; UPDATE: 1, a
+  float alpha, beta;      // GRAM: 1, -; POLY: c, b; UPDATE: 1, a (3xTF32) or - (bf16)
+  float diag;             // added to the diagonal of the output: bf16 POLY a (B' = a I + B), else 0
   const float* scale;     // per bucket-local matrix
   DeviceStatus* status;
   // tile schedule: cluster c runs tiles sched_units[sched_off[c] .. sched_off[c+1])

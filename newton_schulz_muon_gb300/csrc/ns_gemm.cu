@@ -10,12 +10,16 @@
 //                                upper part and mirrors it into the lower part.
 //   POLY   B  = c (A A) + b A    m x m, symmetric (a polynomial of A); A A is read
 //                                as A A^T so both operands are K-major rows; the
-//                                b A term is added in the epilogue.
-//   UPDATE X' = (B X) + a X      m x n; B rows are K-major; bf16 reads X MN-major
-//                                (n contiguous); 3xTF32 reads the rows of X^T
-//                                (K-major, kept beside X in that mode) and also
-//                                writes X'^T.  The a X term is added in the
+//                                b A term is added in the epilogue, and in bf16
+//                                also a on the diagonal: B' = a I + B.
+//   UPDATE X' = B' X (bf16)      m x n; B rows are K-major; bf16 reads X MN-major
+//          X' = (B X) + a X      (n contiguous); 3xTF32 reads the rows of X^T
+//          (3xTF32)              (K-major, kept beside X in that mode), writes
+//                                X'^T as well, and adds the a X term in the
 //                                epilogue.
+// Folding a I into B changes only where bf16 rounding falls: near convergence B'
+// has eigenvalues near 1 where B has them near a - 1, so rounding B' to bf16 loses
+// less than rounding B, and the UPDATE epilogue reads no addend.
 //
 // In the first iteration X holds the un-normalised V; the per-matrix factor
 // s = 1/(||V||_F + eps) is applied in the epilogues (GRAM: s^2, UPDATE: s).  The
@@ -533,7 +537,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     const int s_end = a.sched_off[cluster_id + 1];
     // addend chunks are requested in the order they are used, one ahead, across
     // tiles: request q lands in slot q % 2 and completes phase (q / 2) % 2
-    const bool has_d = !kTF32 && mode != kGram;
+    const bool has_d = !kTF32 && mode == kPoly;
     int d_req = 0, d_use = 0;
     auto d_request = [&](const GemmGroup& Gx, int b, int64_t r0, int64_t c) {
       const int s = d_req & 1;
@@ -629,6 +633,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
             }
             __syncwarp();  // the addend slot and rowbuf are refilled next
             continue;
+          }
+          if (c0 == row0 && a.diag != 0.f) {  // a chunk on the diagonal: element (lane, lane)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j == lane) v[j] += a.diag;
           }
           // In the symmetric modes only the upper triangle is stored, and its
           // mirror: a chunk below the diagonal stores nothing, one above it goes

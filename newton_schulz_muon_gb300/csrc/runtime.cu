@@ -597,8 +597,11 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
       ga.mode = mode;
       ga.n_groups = (int32_t)b.groups.size();
       ga.use_scale = it == 0 && mode != kPoly ? 1 : 0;
+      // bf16: the a X term rides in B' = a I + b A + c A A (POLY adds a on the
+      // diagonal), so UPDATE is the plain product B' X; 3xTF32 adds a X in UPDATE
       ga.alpha = mode == kPoly ? c.ns_c : 1.0f;
-      ga.beta = mode == kPoly ? c.ns_b : (mode == kUpdate ? c.ns_a : 0.0f);
+      ga.beta = mode == kPoly ? c.ns_b : (mode == kUpdate && tf32 ? c.ns_a : 0.0f);
+      ga.diag = mode == kPoly && !tf32 ? c.ns_a : 0.0f;
       ga.scale = at<float>(p, p->off_scale);
       ga.status = at<DeviceStatus>(p, p->off_status);
       const int32_t* sched = reinterpret_cast<const int32_t*>(p->ws + p->off_sched + b.sched_off[mode]);
