@@ -302,9 +302,13 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   return r;
 }
 
-// Arrive on a barrier given by its shared::cluster address (possibly in a peer CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Arrive on a barrier given by its shared::cluster address (possibly in a peer
+// CTA), without release ordering: for signals that order nothing but operations
+// the caller has already waited for (such as tcgen05.ld followed by
+// tcgen05.wait::ld and tcgen05.fence::before_thread_sync).  A release at cluster
+// scope would first wait for the thread's earlier global and bulk stores.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 3-D tiled load into this CTA's shared memory whose completion is signalled on a
@@ -352,11 +356,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor for kind::f16 / kind::tf32: D fp32 (bits 4-5 = 1),
-// A/B format (bits 7-9, 10-12: 1 = bf16, 2 = tf32), A K-major (bit 15 = 0),
-// B major (bit 16: 0 = K-major, 1 = MN-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// A/B format (bits 7-9, 10-12: 1 = bf16, 2 = tf32), A major (bit 15) and B major
+// (bit 16): 0 = K-major, 1 = MN-major; N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t m, uint32_t n,
-                                                  uint32_t b_mn_major) {
-  return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (b_mn_major << 16) |
+                                                  uint32_t b_mn_major, uint32_t a_mn_major = 0u) {
+  return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (a_mn_major << 15) | (b_mn_major << 16) |
          ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 

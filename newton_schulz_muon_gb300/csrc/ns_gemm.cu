@@ -6,13 +6,12 @@
 // full 2-D matrix; "Muon Optimizer + FSDP", section 背景):
 //
 //   GRAM   A  = X X^T            m x m, symmetric: only tiles touching the upper
-//                                triangle are computed; the epilogue writes the
-//                                upper part and mirrors it into the lower part.
+//                                triangle are computed.
 //   POLY   B  = c (A A) + b A    m x m, symmetric (a polynomial of A); A A is read
-//                                as A A^T so both operands are K-major rows; the
-//                                b A term is added in the epilogue, and in bf16
-//                                also a on the diagonal: B' = a I + B.
-//   UPDATE X' = B' X (bf16)      m x n; B rows are K-major; bf16 reads X MN-major
+//                                as A A^T (both operands rows of A); the b A term
+//                                is added in the epilogue, and in bf16 also a on
+//                                the diagonal: B' = a I + B.
+//   UPDATE X' = B' X (bf16)      m x n; B rows are the A operand; bf16 reads X MN-major
 //          X' = (B X) + a X      (n contiguous); 3xTF32 reads the rows of X^T
 //          (3xTF32)              (K-major, kept beside X in that mode), writes
 //                                X'^T as well, and adds the a X term in the
@@ -20,6 +19,18 @@
 // Folding a I into B changes only where bf16 rounding falls: near convergence B'
 // has eigenvalues near 1 where B has them near a - 1, so rounding B' to bf16 loses
 // less than rounding B, and the UPDATE epilogue reads no addend.
+//
+// Symmetric storage.  bf16 A is stored as exactly the tiles computed: the
+// 256 x 256 blocks on and above the diagonal, each written whole.  Element (i, k)
+// is held at (i, k) when i / 256 <= k / 256 and at (k, i) otherwise, so POLY reads
+// a 64-deep k block of an operand in place (K-major rows) when the block lies in
+// or right of the operand rows' 256-block, and from the transposed position
+// (MN-major, rows of the block contiguous) when it lies left of it; the tensor
+// core takes either major per instruction.  POLY writes B' whole (its tiles above
+// the diagonal blocks also as their transposes), because transposed reads of the
+// A operand slow UPDATE's mainloop more than the extra boxes cost POLY's epilogue
+// (measured on one Qwen3-4B layer and on a 169-matrix bucket of 768 x 2048).
+// 3xTF32 keeps full symmetric matrices (upper part mirrored) and K-major reads.
 //
 // In the first iteration X holds the un-normalised V; the per-matrix factor
 // s = 1/(||V||_F + eps) is applied in the epilogues (GRAM: s^2, UPDATE: s).  The
@@ -43,8 +54,8 @@
 //                   warp owns 8 KB of shared memory through which its 32 x 32
 //                   chunks pass as TMA boxes -- the addend is requested one
 //                   chunk ahead (across tiles) into two slots with their own
-//                   mbarriers, the output and the mirror's transpose leave as
-//                   TMA stores, and the last UPDATE's weights move by cp.async.
+//                   mbarriers, the output leaves as TMA stores, and the last
+//                   UPDATE's weights move by cp.async, one chunk ahead.
 // Tiles of all same-shape groups of a micro-bucket (and of all its matrices) are
 // numbered in one space; a host-computed longest-processing-time schedule gives
 // each cluster its list of tiles.
@@ -84,9 +95,9 @@ struct Cfg {
   static constexpr int kBRows = kBN / kCL;                // B rows (or columns) held by one CTA
   static constexpr uint32_t kB = kBRows * 128;            // 32 KB or 16 KB
   static constexpr uint32_t kStage = kParts * (kA + kB);
-  // bf16 epilogue: per epilogue warp 8 KB -- the output chunk (32 x 32 bf16)
-  // and its transpose, or the weights of the last UPDATE; and two addend chunks
-  // (the current one and the next, TMA boxes)
+  // bf16 epilogue: per epilogue warp 8 KB -- the output chunk (32 x 32 bf16) and
+  // two addend chunks (the current one and the next, TMA boxes), or two 32 x 32
+  // chunks of the last UPDATE's weights
   static constexpr uint32_t kWarpStaging = 8192u;
   static constexpr uint32_t kStaging = kTF32 ? 0u : 8u * kWarpStaging;
   // as many stages as fit in the 227 KB of dynamic shared memory a CTA may use
@@ -390,6 +401,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
   const uint32_t tmem_base = tmem_slot;
   const int mode = a.mode;
   const bool mn_b = (mode == kUpdate) && !kTF32;  // B operand read MN-major
+  // bf16 A holds only its 256-blocks on or above the diagonal; POLY's operands
+  // (both rows of A) read each k block that lies left of their rows' 256-block
+  // transposed, from the stored part
+  const bool sym_a = !kTF32 && mode == kPoly;
+  const bool sym_b = sym_a;
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
@@ -412,14 +428,32 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], C::kTx);
           const uint32_t bar = kCL > 1 ? mapa_shared(&full_bar[stage], 0) : smem_u32(&full_bar[stage]);
           const int k0 = kb * C::kBK;
+          const int i0 = tc.bi * kBM;                                  // first row of operand A
+          const int j0 = tc.bj * kBN + (kCL > 1 ? rank * C::kBRows : 0);  // first row of operand B
+          const bool a_low = sym_a && (k0 >> 8) < (i0 >> 8);
+          const bool b_low = sym_b && (k0 >> 8) < (j0 >> 8);
+          if (a_low || b_low) {
+            // transposed reads: 64-row chunks of the operand, each a {64, 64} box
+            if (a_low)
+              for (int q = 0; q < kBM / C::kBK; ++q) {
+                if constexpr (kCL == 1) tma_load_3d(sa + q * C::kChunkBytes, &G.map_a_mn, &full_bar[stage], i0 + q * C::kBK, k0, tc.b);
+                else tma_load_3d_pair(sa + q * C::kChunkBytes, &G.map_a_mn, bar, i0 + q * C::kBK, k0, tc.b);
+              }
+            if (b_low)
+              for (int q = 0; q < C::kChunks; ++q) {
+                if constexpr (kCL == 1) tma_load_3d(sb + q * C::kChunkBytes, &G.map_b_mn, &full_bar[stage], j0 + q * C::kBK, k0, tc.b);
+                else tma_load_3d_pair(sb + q * C::kChunkBytes, &G.map_b_mn, bar, j0 + q * C::kBK, k0, tc.b);
+              }
+          }
 #pragma unroll
           for (int part = 0; part < C::kParts; ++part) {
             const CUtensorMap* ma = part ? &G.map_a_lo : &G.map_a;
             const CUtensorMap* mb = part ? &G.map_b_lo : &G.map_b;
             uint8_t* sbp = sb + part * C::kB;
             if constexpr (kCL == 1) {
-              tma_load_3d(sa + part * C::kA, ma, &full_bar[stage], k0, tc.bi * kBM, tc.b);
-              if (mn_b) {
+              if (!a_low) tma_load_3d(sa + part * C::kA, ma, &full_bar[stage], k0, tc.bi * kBM, tc.b);
+              if (b_low) {
+              } else if (mn_b) {
 #pragma unroll
                 for (int q = 0; q < C::kChunks; ++q)
                   tma_load_3d(sbp + q * C::kChunkBytes, mb, &full_bar[stage], tc.bj * kBN + q * C::kBK, k0, tc.b);
@@ -430,8 +464,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
               }
             } else {
               // own 128 rows of A and own half of B, completing on the even CTA's barrier
-              tma_load_3d_pair(sa + part * C::kA, ma, bar, k0, tc.bi * kBM, tc.b);
-              if (mn_b) {
+              if (!a_low) tma_load_3d_pair(sa + part * C::kA, ma, bar, k0, tc.bi * kBM, tc.b);
+              if (b_low) {
+              } else if (mn_b) {
 #pragma unroll
                 for (int q = 0; q < C::kChunks; ++q)
                   tma_load_3d_pair(sbp + q * C::kChunkBytes, mb, bar, tc.bj * kBN + rank * C::kBRows + q * C::kBK,
@@ -479,11 +514,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           if (lane == 0) {
             const uint32_t sa = smem_u32(smem + (size_t)stage * C::kStage);
             const uint32_t sb = sa + C::kParts * C::kA;
+            // the same k-block choice as the producer's (both CTAs of a pair share
+            // the row block of A and the column block of B)
+            const int k0 = kb * C::kBK;
+            const bool a_low = sym_a && (k0 >> 8) < ((tc.bi * kBM) >> 8);
+            const bool b_low = sym_b && (k0 >> 8) < ((tc.bj * kBN) >> 8);
+            const bool b_t = mn_b || b_low;
+            const uint32_t id = make_idesc(C::kFormat, kBM * kCL, kBN, b_t ? 1u : 0u, a_low ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < C::kBK / C::kInstK; ++kk) {
-              const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
-              const uint64_t bd = mn_b ? smem_desc_sw128(sb + kk * C::kInstK * 128, C::kChunkBytes, 1024)
-                                       : smem_desc_sw128(sb + kk * 32, 16, 1024);
+              const uint64_t ad = a_low ? smem_desc_sw128(sa + kk * C::kInstK * 128, C::kChunkBytes, 1024)
+                                        : smem_desc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = b_t ? smem_desc_sw128(sb + kk * C::kInstK * 128, C::kChunkBytes, 1024)
+                                      : smem_desc_sw128(sb + kk * 32, 16, 1024);
               const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
               if constexpr (kTF32) {
                 const uint64_t ad_lo = smem_desc_sw128(sa + C::kA + kk * 32, 16, 1024);
@@ -492,7 +535,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
                 mma<true, kCL>(d_tmem, ad, bd_lo, idesc, 1u);
                 mma<true, kCL>(d_tmem, ad, bd, idesc, 1u);
               } else {
-                mma<false, kCL>(d_tmem, ad, bd, idesc, accumulate);
+                mma<false, kCL>(d_tmem, ad, bd, id, accumulate);
               }
             }
             if constexpr (kCL > 1) mma_commit_multicast<kCL>(&empty_bar[stage], kPair);
@@ -524,12 +567,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     const int ew = warp - 2;
-    // bf16 staging of this warp (after the ring), every buffer one 32 x 32 box in
-    // the 64-byte swizzle: the output chunk and its transpose (or the last
-    // UPDATE's weights), and two addend slots filled by TMA
+    // bf16 staging of this warp (after the ring), in 32 x 32 boxes of the 64-byte
+    // swizzle: the output chunk and its transpose (first 4 KB) and two POLY
+    // addend slots filled by TMA (last 4 KB); the last UPDATE uses the two halves
+    // as weight slots instead
     uint8_t* wst = smem + (size_t)C::kStages * C::kStage + (size_t)ew * C::kWarpStaging;
     uint4* rowbuf = reinterpret_cast<uint4*>(wst);
-    __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(wst + 2048u);
+    __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(wst + 2048u);  // POLY: the chunk transposed
     uint4* dbuf = reinterpret_cast<uint4*>(wst + 4096u);  // addend slot s at dbuf + s * 128
     uint64_t* dbar = &addend_bar[2 * ew];
     const uint32_t tempty_lead[2] = {kCL > 1 ? mapa_shared(&tempty_bar[0], 0) : 0u,
@@ -547,6 +591,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       }
       ++d_req;
     };
+    // last UPDATE: the weights of staged chunk q arrive by cp.async in slot q % 2
+    // (the first or the second 4 KB of the staging, free of addends in UPDATE),
+    // one cp.async group per chunk, requested one chunk ahead across tiles
+    int w_req = 0, w_use = 0;
+    auto w_slot = [&](int q) { return reinterpret_cast<uint4*>(wst + (q & 1) * 4096u); };
     int acc = 0;
     uint32_t acc_phase = 0;
     bool failed = false;
@@ -566,7 +615,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
         // the first addend chunk loads while the accumulator is awaited, unless
         // the previous tile requested it already
         if (has_d && nch > 0 && d_req == d_use) d_request(G, tc.b, row0, c_first);
-        if (a.fuse_apply) stg = staged_target(a.apply, G.mat_base + tc.b);
+        if (a.fuse_apply) {
+          stg = staged_target(a.apply, G.mat_base + tc.b);
+          if (stg.ok && nch > 0 && w_req == w_use) {  // not requested by the previous tile
+            staged_load(a.apply, stg, G.M, G.N, row0, c_first, lane, w_slot(w_req++));
+            cp_async_commit();
+          }
+        }
       }
       // warp-uniform decision: tcgen05.ld below needs every lane of the warp
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_p, status);
@@ -585,8 +640,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
         const int64_t c0 = (int64_t)tc.bj * kBN + cc * 32;
         if constexpr (!kTF32) {
           const bool staged = a.fuse_apply && stg.ok;
-          if (staged) staged_load(a.apply, stg, G.M, G.N, row0, c0, lane, rowbuf);
-          cp_async_commit();
           // the next addend chunk: this tile's next, else the next tile's first
           if (has_d && d_req == d_use + 1) {
             if (k + 1 < nch) {
@@ -600,6 +653,24 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           }
           float v[32];
           tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kBN + cc * 32), v);
+          if (staged && w_req == w_use + 1) {
+            // the next chunk's weights (this tile's next chunk, else the next tile's
+            // first), requested after the accumulator load, which would otherwise
+            // queue behind these copies
+            if (k + 1 < nch) {
+              staged_load(a.apply, stg, G.M, G.N, row0, c0 + 32, lane, w_slot(w_req++));
+              cp_async_commit();
+            } else if (si + 1 < s_end) {
+              const TileCoord tn = decode_tile<kCL>(a, a.sched_units[si + 1], rank);
+              const GemmGroup& Gn = a.g[tn.g];
+              const int64_t cn = (int64_t)tn.bj * kBN + half * (kBN / 2);
+              const StagedTarget sn = staged_target(a.apply, Gn.mat_base + tn.b);
+              if (sn.ok && cn < Gn.N) {
+                staged_load(a.apply, sn, Gn.M, Gn.N, (int64_t)tn.bi * kBM + quad * 32, cn, lane, w_slot(w_req++));
+                cp_async_commit();
+              }
+            }
+          }
           const bool row_ok = r < G.M;
           const int64_t valid = G.N - c0;
           if (has_d) {
@@ -625,13 +696,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           }
           if (a.fuse_apply) {  // last iteration: update the weights directly, X is not stored
             if (staged) {
-              cp_async_wait<0>();
+              // this chunk's group is the oldest; the next chunk's may stay in flight
+              if (w_req - w_use > 1) cp_async_wait<1>(); else cp_async_wait<0>();
               __syncwarp();
-              staged_update_store(a.apply, stg, G.M, G.N, row0, c0, lane, v, rowbuf);
+              staged_update_store(a.apply, stg, G.M, G.N, row0, c0, lane, v, w_slot(w_use++));
             } else if (row_ok) {
               fused_apply_chunk(a.apply, G.mat_base + tc.b, r, c0, valid, v);
             }
-            __syncwarp();  // the addend slot and rowbuf are refilled next
+            __syncwarp();  // this weight slot is refilled two chunks later
             continue;
           }
           if (c0 == row0 && a.diag != 0.f) {  // a chunk on the diagonal: element (lane, lane)
@@ -639,58 +711,34 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
             for (int j = 0; j < 32; ++j)
               if (j == lane) v[j] += a.diag;
           }
-          // In the symmetric modes only the upper triangle is stored, and its
-          // mirror: a chunk below the diagonal stores nothing, one above it goes
-          // out as two TMA boxes (the chunk and its transpose), one on the
-          // diagonal element by element.
-          if (row0 >= G.M || (sym && c0 + 32 <= row0)) {
+          // Every chunk of a tile leaves as one TMA box.  GRAM stores A as the
+          // 256-blocks its tiles cover (on and above the diagonal), which POLY
+          // reads transposed where needed; POLY also writes the transpose of a
+          // chunk above the diagonal blocks (row block left of the column block),
+          // so that B' is whole and UPDATE reads its rows in place.
+          if (row0 >= G.M) {
             __syncwarp();
             continue;
           }
+          const bool mirror = mode == kPoly && (row0 >> 8) < (c0 >> 8);
           if (lane == 0) bulk_wait_group_read<0>();  // the last boxes have left the staging
           __syncwarp();
 #pragma unroll
           for (int q = 0; q < 4; ++q) rowbuf[unit4(lane, q)] = pack8v(v + 8 * q);
-          if (sym) {
+          if (mirror) {
             // row j of the transpose is column j of the chunk; lane = its element
             const int e = lane & 7, u = lane >> 3;
 #pragma unroll
             for (int j = 0; j < 32; ++j) tbuf[j * 32 + ((u ^ ((j >> 1) & 3)) << 3) + e] = __float2bfloat16_rn(v[j]);
           }
-          if (!sym || c0 >= row0 + 32) {
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(&G.map_c, rowbuf, (int)c0, (int)row0, tc.b);
-              if (sym) tma_store_3d(&G.map_c, tbuf, (int)row0, (int)c0, tc.b);
-              bulk_commit_group();
-            }
-            __syncwarp();
-            continue;
-          }
-          // diagonal chunk (c0 == row0): the upper part, and its mirror C[c][r] for c > r
+          fence_proxy_async_shared();
           __syncwarp();
-          __nv_bfloat16* Cm = reinterpret_cast<__nv_bfloat16*>(G.c_hi) + mb;
-          const uint4* tb4 = reinterpret_cast<const uint4*>(tbuf);
-          const int g = lane & 3;
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const int i = 8 * qq + (lane >> 2);
-            const int64_t rr = row0 + i, cg = c0 + 8 * g;
-            const uint4 val = rowbuf[unit4(i, g)];
-            const uint4 tv = tb4[unit4(i, g)];
-            const __nv_bfloat16* ev = reinterpret_cast<const __nv_bfloat16*>(&val);
-            const __nv_bfloat16* et = reinterpret_cast<const __nv_bfloat16*>(&tv);
-            // direct: row rr, columns cg .. cg + 7 with column >= row
-            // mirror: row c0 + i, columns row0 + 8g .. +7 with column < row
-#pragma unroll
-            for (int h = 0; h < 8; ++h) {
-              if (rr < G.M && cg + h < G.N && cg + h >= rr) Cm[rr * ld + cg + h] = ev[h];
-              const int64_t mr = c0 + i, mc = row0 + 8 * g + h;
-              if (mr < G.N && mc < G.M && mc < mr) Cm[mr * ld + mc] = et[h];
-            }
+          if (lane == 0) {
+            tma_store_3d(&G.map_c, rowbuf, (int)c0, (int)row0, tc.b);
+            if (mirror) tma_store_3d(&G.map_c, tbuf, (int)row0, (int)c0, tc.b);
+            bulk_commit_group();
           }
-          __syncwarp();  // the buffers are rewritten by the next chunk
+          __syncwarp();
           continue;
         } else {
           float v[32];
@@ -739,7 +787,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
         mbar_arrive(&tempty_bar[acc]);
       } else {
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty_lead[acc]);  // release the accumulator to the MMA issuer
+        // hand the accumulator back to the MMA issuer: this warp's tcgen05.ld have
+        // completed (wait::ld) and are ordered before the arrive by the fence above
+        if (lane == 0) mbar_arrive_cluster_relaxed(tempty_lead[acc]);
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
