@@ -23,6 +23,12 @@ and follows the steps in the order the sources give them:
   "first-order momentum tracking"); the reading is the EMA form
   M <- mu M + (1 - mu) G with Nesterov blend V = (1 - mu) G + mu M_new,
   and the SGD form M <- mu M + G, V = G + mu M_new as an option.
+* per-iteration coefficients -- DeepSpeed issue "[RFC] Enable Correct and
+  High-Performance Muon Optimizer under ZeRO CPU Offload", follow-up list
+  ("Polar Express" as an ns_method): iteration k may use its own (a_k, b_k, c_k);
+  ``polar_express_schedule`` builds them by fitting, at each iteration, the odd
+  quintic closest to 1 in the max norm on the interval holding the singular
+  values, then carrying the interval forward (the pages give no coefficients).
 * apply -- W <- W - lr (sqrt(max(1, rows/cols)) U + wd W), decoupled weight
   decay on the old W.
 * fused tensors -- "Muon Optimizer + FSDP", section 分块通信 (chunked
@@ -31,8 +37,8 @@ and follows the steps in the order the sources give them:
   Muon on interleaved [Q0, K0, V0, Q1, ...] layouts runs one Newton-Schulz per
   head slice.
 
-Pins (tests/test_oracle_pins.py) tie these functions to mathematics that does
-not go through them: the SVD closed form of an odd matrix polynomial,
+Pins (tests/test_oracle_pins.py, tests/test_oracle_schedule_pins.py) tie these
+functions to mathematics that does not go through them: the SVD closed form of an odd matrix polynomial,
 orthogonal equivariance, scale and transpose identities, per-shard vs whole
 matrix, and closed forms of the momentum recursion.
 """
@@ -119,19 +125,122 @@ def ns_iteration(X: np.ndarray, a: float, b: float, c: float) -> np.ndarray:
     return a * X + B @ X
 
 
-def newton_schulz(V, steps: int = DEFAULT_NS_STEPS, coeffs: Sequence[float] = DEFAULT_COEFFS,
+def coefficient_schedule(coeffs, steps: int) -> List[Tuple[float, float, float]]:
+    """The (a, b, c) of each of ``steps`` iterations: one triple used every time,
+    or a per-iteration list of triples whose last entry repeats past its end."""
+    flat = list(coeffs)
+    if flat and not isinstance(flat[0], (tuple, list, np.ndarray)):
+        triples = [tuple(float(v) for v in flat)]
+    else:
+        triples = [tuple(float(v) for v in t) for t in flat]
+    if any(len(t) != 3 for t in triples) or not triples:
+        raise ValueError("coefficients are (a, b, c) triples")
+    return [triples[min(k, len(triples) - 1)] for k in range(int(steps))]
+
+
+def newton_schulz(V, steps: int = DEFAULT_NS_STEPS, coeffs=DEFAULT_COEFFS,
                   eps: float = DEFAULT_EPS) -> np.ndarray:
     """Approximate orthogonal polar factor of the whole 2-D matrix V (fp64).
 
     Orient wide, normalise by the Frobenius norm, run ``steps`` quintic
-    iterations, and undo the orientation.
+    iterations, and undo the orientation.  ``coeffs`` is one (a, b, c) for every
+    iteration or a per-iteration schedule (see ``coefficient_schedule``).
     """
-    a, b, c = (float(v) for v in coeffs)
     X, transposed = orient(V)
     X = frobenius_normalize(X, eps)
-    for _ in range(int(steps)):
+    for a, b, c in coefficient_schedule(coeffs, steps):
         X = ns_iteration(X, a, b, c)
     return X.T if transposed else X
+
+
+# ---------------------------------------------------------------------------
+# per-iteration coefficients (DeepSpeed issue "[RFC] Enable Correct and
+# High-Performance Muon Optimizer under ZeRO CPU Offload", follow-up list:
+# Newton-Schulz with per-iteration optimised coefficients, "Polar Express",
+# arXiv:2505.16932, as an ns_method option)
+# ---------------------------------------------------------------------------
+# The pages name the method and its aim -- fewer iterations to the same polar
+# accuracy -- but print no coefficients.  The construction taken here is the
+# plainest reading of "per-iteration optimised": iteration k uses the odd quintic
+# p_k(x) = a x + b x^3 + c x^5 that minimises max |1 - p_k(x)| over the interval
+# [l_k, u_k] known to hold the singular values, and the next interval is the
+# image [1 - E_k, 1 + E_k] of that one (E_k the minimised error).  After the
+# Frobenius normalisation u_0 = 1; l_0 is an assumed lower bound.
+
+def minimax_odd_quintic(lo: float, hi: float, grid_points: int = 200001, max_iter: int = 60):
+    """(a, b, c, E): the odd quintic closest to 1 in the max norm on [lo, hi].
+
+    Exchange iteration on the three-function basis x, x^3, x^5: on a reference of
+    four points solve p(x_i) + (-1)^i E = 1, then move the reference to the
+    extrema of the error 1 - p found on a dense grid, until the largest error on
+    the grid equals |E|.  E > 0 means the error is +|E| at ``lo``.
+    """
+    lo, hi = float(lo), float(hi)
+    if not 0.0 < lo <= hi:
+        raise ValueError("need 0 < lo <= hi")
+    x = np.linspace(lo, hi, grid_points)
+    if hi - lo < 1e-6:
+        # the three basis functions are numerically dependent on so short an
+        # interval; the minimax quintic there tends to the one flat to third order
+        # at 1, p(x) = (15 x - 10 x^3 + 3 x^5) / 8 (p(1) = 1, p'(1) = p''(1) = 0)
+        a, b, c = 15.0 / 8.0, -10.0 / 8.0, 3.0 / 8.0
+        err = 1.0 - (a * x + b * x ** 3 + c * x ** 5)
+        return a, b, c, float(err[np.argmax(np.abs(err))])
+    ref = lo + (hi - lo) * (1.0 - np.cos(np.pi * np.arange(4) / 3.0)) / 2.0
+    sign = (-1.0) ** np.arange(4)
+    for _ in range(max_iter):
+        sol = np.linalg.solve(np.column_stack([ref, ref ** 3, ref ** 5, sign]), np.ones(4))
+        a, b, c, E = (float(v) for v in sol)
+        err = 1.0 - (a * x + b * x ** 3 + c * x ** 5)
+        # the error's local extrema on the grid, ends included
+        d = np.diff(err)
+        turn = np.where(np.sign(d[1:]) != np.sign(d[:-1]))[0] + 1
+        idx = np.concatenate([[0], turn, [len(x) - 1]])
+        # keep one point per run of equal sign: the largest magnitude
+        pts = []
+        for i in idx:
+            if pts and np.sign(err[i]) == np.sign(err[pts[-1]]):
+                if abs(err[i]) > abs(err[pts[-1]]):
+                    pts[-1] = i
+            else:
+                pts.append(i)
+        while len(pts) > 4:  # drop the smaller end
+            pts.pop(0 if abs(err[pts[0]]) < abs(err[pts[-1]]) else -1)
+        if len(pts) < 4:
+            raise RuntimeError("the error does not alternate four times")
+        # sharpen interior extrema with Newton steps on p'(x) = a + 3 b x^2 + 5 c x^4
+        ref = x[pts].copy()
+        for i in range(1, 3):
+            t = ref[i]
+            for _ in range(8):
+                d1 = a + 3 * b * t * t + 5 * c * t ** 4
+                d2 = 6 * b * t + 20 * c * t ** 3
+                if d2 == 0.0:
+                    break
+                t = min(max(t - d1 / d2, lo), hi)
+            ref[i] = t
+        e_ref = 1.0 - (a * ref + b * ref ** 3 + c * ref ** 5)
+        sign = np.sign(e_ref)
+        worst = max(float(np.max(np.abs(err))), float(np.max(np.abs(e_ref))))
+        if worst - abs(E) <= 1e-14 * max(1.0, abs(E)):
+            break
+    # report the largest error actually reached, so that the next interval holds
+    # the image of this one
+    return a, b, c, math.copysign(worst, E)
+
+
+def polar_express_schedule(n_iters: int, lower: float = 1e-3, safety: float = 1.0):
+    """Per-iteration (a, b, c) for ``n_iters`` iterations and the bound E_k after
+    each: iteration k fits [l_k, u_k * safety] (safety >= 1 leaves room for
+    rounding that pushes a singular value past u_k); then [l, u] = [1 - E, 1 + E]."""
+    lo, hi = float(lower), 1.0
+    coeffs, errs = [], []
+    for _ in range(int(n_iters)):
+        a, b, c, E = minimax_odd_quintic(lo, hi * float(safety))
+        coeffs.append((a, b, c))
+        errs.append(abs(E))
+        lo, hi = 1.0 - abs(E), 1.0 + abs(E)
+    return coeffs, errs
 
 
 # ---------------------------------------------------------------------------
