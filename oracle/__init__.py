@@ -179,10 +179,12 @@ def minimax_odd_quintic(lo: float, hi: float, grid_points: int = 200001, max_ite
     if not 0.0 < lo <= hi:
         raise ValueError("need 0 < lo <= hi")
     x = np.linspace(lo, hi, grid_points)
-    if hi - lo < 1e-6:
-        # the three basis functions are numerically dependent on so short an
-        # interval; the minimax quintic there tends to the one flat to third order
-        # at 1, p(x) = (15 x - 10 x^3 + 3 x^5) / 8 (p(1) = 1, p'(1) = p''(1) = 0)
+    if hi - lo < 1e-4:
+        # the three basis functions are nearly dependent on so short an interval
+        # (fits differ in their coefficients, not in their ~1e-13 errors); the
+        # minimax quintic there tends to the one flat to third order at 1,
+        # p(x) = (15 x - 10 x^3 + 3 x^5) / 8 (p(1) = 1, p'(1) = p''(1) = 0), whose
+        # error on [1 - d, 1 + d] is about 2.5 d^3
         a, b, c = 15.0 / 8.0, -10.0 / 8.0, 3.0 / 8.0
         err = 1.0 - (a * x + b * x ** 3 + c * x ** 5)
         return a, b, c, float(err[np.argmax(np.abs(err))])
