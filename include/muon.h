@@ -69,6 +69,9 @@ typedef int32_t muon_status;
                                  other buckets run three grouped GEMM launches per iteration */
 #define MUON_NS_KERNEL_GEMM 1 /* always the grouped GEMM launches */
 
+/* Newton-Schulz iterations per step: ns_steps in [0, MUON_MAX_NS_STEPS] */
+#define MUON_MAX_NS_STEPS 16
+
 /* momentum form (the pages name momentum_update without a formula) */
 #define MUON_MOMENTUM_EMA 0 /* M <- mu M + (1-mu) G;  Nesterov V = (1-mu) G + mu M */
 #define MUON_MOMENTUM_SGD 1 /* M <- mu M + G;         Nesterov V = G + mu M        */
@@ -132,6 +135,30 @@ muon_status muon_plan_workspace_bytes(const muon_plan_t* plan, size_t* device_by
  * enqueued step.  Errors: MUON_ERR_INVALID, MUON_ERR_NO_WORKSPACE, MUON_ERR_CUDA,
  * MUON_ERR_UNSUPPORTED (device is not sm_103). */
 muon_status muon_plan_bind_workspace(muon_plan_t* plan, void* dev_ptr, size_t bytes);
+
+/* Per-iteration Newton-Schulz coefficients for later muon_step and
+ * muon_offload_step calls on this plan (DeepSpeed issue "[RFC] Enable Correct and
+ * High-Performance Muon Optimizer under ZeRO CPU Offload", follow-up list:
+ * per-iteration optimised coefficients as an ns_method option).
+ *   coeffs[3k], coeffs[3k+1], coeffs[3k+2]: (a_k, b_k, c_k) of iteration k, host
+ *   memory, copied; iterations past n_iters reuse the last triple.
+ *   n_iters: 1..MUON_MAX_NS_STEPS, or 0 (coeffs may be NULL) to return to the
+ *   plan's cfg (ns_a, ns_b, ns_c) for every iteration.
+ * Non-finite values and out-of-range n_iters return MUON_ERR_INVALID and leave the
+ * plan unchanged.  Not to be called while a step of this plan is being enqueued. */
+muon_status muon_set_ns_schedule(muon_plan_t* plan, const float* coeffs, int32_t n_iters);
+
+/* Builds a per-iteration schedule by the greedy minimax construction: iteration
+ * k uses the odd quintic p_k(x) = a x + b x^3 + c x^5 minimising max |1 - p_k(x)|
+ * over [l_k, safety * u_k], and [l_{k+1}, u_{k+1}] = [1 - E_k, 1 + E_k] with E_k
+ * that minimum, from [lower, 1] (singular values after the Frobenius
+ * normalisation lie in (0, 1]).  Host only, no device or plan involved.
+ *   n_iters: 1..MUON_MAX_NS_STEPS; lower in (0, 1); safety in [1, 2].
+ *   coeffs_out[3 n_iters]: (a_k, b_k, c_k), fp32.
+ *   err_out[n_iters] (nullable): E_k, the bound |1 - p_k o ... o p_0(x)| <= E_k
+ *   for x in [lower, 1]. */
+muon_status muon_polar_express_coefficients(int32_t n_iters, double lower, double safety, float* coeffs_out,
+                                            double* err_out);
 
 /* One Muon step over every matrix of the plan, enqueued on `stream`.
  *   params[n_mats]:   device pointers, weights (cfg.param_dtype), updated in place.

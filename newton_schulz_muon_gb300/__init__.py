@@ -35,6 +35,7 @@ MUON_MOMENTUM_EMA = 0
 MUON_MOMENTUM_SGD = 1
 MUON_NS_KERNEL_AUTO = 0
 MUON_NS_KERNEL_GEMM = 1
+MUON_MAX_NS_STEPS = 16
 
 
 class muon_shape(ctypes.Structure):
@@ -85,6 +86,9 @@ def _load() -> ctypes.CDLL:
         "muon_sync": (c_int32, [P, P, POINTER(c_int64)]),
         "muon_get_plan_info": (c_int32, [P, POINTER(muon_plan_info)]),
         "muon_get_bucket_info": (c_int32, [P, c_int64, POINTER(muon_bucket_info)]),
+        "muon_set_ns_schedule": (c_int32, [P, POINTER(c_float), c_int32]),
+        "muon_polar_express_coefficients": (c_int32, [c_int32, ctypes.c_double, ctypes.c_double,
+                                                      POINTER(c_float), POINTER(ctypes.c_double)]),
         "muon_get_stats": (c_int32, [P, POINTER(muon_stats)]),
         "muon_last_error": (c_char_p, []),
         "muon_status_string": (c_char_p, [c_int32]),
@@ -250,6 +254,27 @@ def muon_get_bucket_info(plan: Plan, b: int) -> muon_bucket_info:
     info = muon_bucket_info()
     _check(_lib().muon_get_bucket_info(plan.handle, int(b), byref(info)), "muon_get_bucket_info")
     return info
+
+
+def muon_set_ns_schedule(plan: Plan, coeffs) -> None:
+    """Per-iteration (a, b, c) triples for later steps of the plan; [] restores the
+    configuration's coefficients for every iteration."""
+    flat = [float(v) for t in coeffs for v in t]
+    n = len(flat) // 3
+    if n * 3 != len(flat):
+        raise ValueError("coefficients are (a, b, c) triples")
+    arr = (c_float * max(len(flat), 1))(*flat)
+    _check(_lib().muon_set_ns_schedule(plan.handle, arr if n else None, n), "muon_set_ns_schedule")
+
+
+def muon_polar_express_coefficients(n_iters: int, lower: float = 1e-3, safety: float = 1.0):
+    """(coefficient triples, per-iteration error bounds) of the minimax schedule,
+    computed by the library on the host."""
+    out = (c_float * (3 * int(n_iters)))()
+    err = (ctypes.c_double * int(n_iters))()
+    _check(_lib().muon_polar_express_coefficients(int(n_iters), float(lower), float(safety), out, err),
+           "muon_polar_express_coefficients")
+    return [tuple(out[3 * k:3 * k + 3]) for k in range(int(n_iters))], list(err)
 
 
 def muon_get_stats(plan: Plan) -> muon_stats:

@@ -162,8 +162,8 @@ struct SmallArgs {
   SmallGroup g[kMaxGroups];
   int32_t n_groups;
   int32_t n_units;       // matrices in the launch
-  int32_t ns_steps;      // quintic iterations (>= 1)
-  float a, b, c;         // X' = a X + (b A + c A A) X, A = X X^T
+  int32_t ns_steps;      // quintic iterations (1 .. MUON_MAX_NS_STEPS)
+  float coef[16][3];     // iteration k: (a, b, c) of X' = a X + (b A + c A A) X, A = X X^T
   const float* scale;    // per bucket-local matrix: 1 / (||V||_F + eps), folded into iteration 0
   DeviceStatus* status;
   ApplyArgs apply;       // the last iteration applies the weight update (or emits U')

@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
             float x[8], w[8];
             unpack8(*p, x);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = a.c * v[8 * q + e] + a.b * x[e];
+            for (int e = 0; e < 8; ++e) w[e] = a.coef[k][2] * v[8 * q + e] + a.coef[k][1] * x[e];
             *p = pack8(w);
           }
         }
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         // ---- X' = (s in iteration 0) (B X + a X), chunk by chunk ----
         const bool last = k + 1 == K;
         const float alpha = k == 0 ? s : 1.f;
-        const float beta = a.a * alpha;
+        const float beta = a.coef[k][0] * alpha;
         ApplyTarget tg{};
         bool vec = false;
         if (last) {

@@ -145,6 +145,8 @@ struct muon_plan_s {
   cudaEvent_t step_start = nullptr, step_end = nullptr;
   bool offload_last = false;
   int64_t last_h2d_bytes = 0, last_d2h_bytes = 0;
+  // per-iteration (a, b, c) set by muon_set_ns_schedule; empty: cfg's for every iteration
+  std::vector<float> ns_sched;
 };
 
 namespace {
@@ -544,6 +546,20 @@ bool uses_small_kernel(const muon_config& c, const Bucket& b) {
 
 // Every iteration of a small-matrix bucket in one launch (X updated in place in
 // the workspace's first X buffer), the weight update fused into the last one.
+// (a, b, c) of Newton-Schulz iteration k: the plan's schedule (its last triple
+// past its end), else the configuration's.
+void ns_coeffs(const muon_plan_t* p, int k, float out[3]) {
+  if (p->ns_sched.empty()) {
+    out[0] = p->cfg.ns_a;
+    out[1] = p->cfg.ns_b;
+    out[2] = p->cfg.ns_c;
+    return;
+  }
+  const int n = (int)(p->ns_sched.size() / 3);
+  const int i = k < n ? k : n - 1;
+  for (int j = 0; j < 3; ++j) out[j] = p->ns_sched[3 * i + j];
+}
+
 muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st,
                              const ApplyArgs& fused) {
   const muon_config& c = p->cfg;
@@ -571,9 +587,7 @@ muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cuda
   sa.n_groups = (int32_t)order.size();
   sa.n_units = units;
   sa.ns_steps = ns_steps;
-  sa.a = c.ns_a;
-  sa.b = c.ns_b;
-  sa.c = c.ns_c;
+  for (int k = 0; k < ns_steps && k < MUON_MAX_NS_STEPS; ++k) ns_coeffs(p, k, sa.coef[k]);
   sa.scale = at<float>(p, p->off_scale);
   sa.status = at<DeviceStatus>(p, p->off_status);
   sa.apply = fused;
@@ -600,9 +614,11 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
       ga.use_scale = it == 0 && mode != kPoly ? 1 : 0;
       // bf16: the a X term rides in B' = a I + b A + c A A (POLY adds a on the
       // diagonal), so UPDATE is the plain product B' X; 3xTF32 adds a X in UPDATE
-      ga.alpha = mode == kPoly ? c.ns_c : 1.0f;
-      ga.beta = mode == kPoly ? c.ns_b : (mode == kUpdate && tf32 ? c.ns_a : 0.0f);
-      ga.diag = mode == kPoly && !tf32 ? c.ns_a : 0.0f;
+      float co[3];
+      ns_coeffs(p, it, co);
+      ga.alpha = mode == kPoly ? co[2] : 1.0f;
+      ga.beta = mode == kPoly ? co[1] : (mode == kUpdate && tf32 ? co[0] : 0.0f);
+      ga.diag = mode == kPoly && !tf32 ? co[0] : 0.0f;
       ga.scale = at<float>(p, p->off_scale);
       ga.status = at<DeviceStatus>(p, p->off_status);
       const int32_t* sched = reinterpret_cast<const int32_t*>(p->ws + p->off_sched + b.sched_off[mode]);
@@ -772,6 +788,16 @@ muon_status muon_get_plan_info(const muon_plan_t* plan, muon_plan_info* info) {
     info->max_bucket_bytes = std::max(info->max_bucket_bytes, b.bytes);
   }
   info->workspace_bytes = plan->ws_bytes;
+  return MUON_OK;
+}
+
+muon_status muon_set_ns_schedule(muon_plan_t* plan, const float* coeffs, int32_t n_iters) {
+  if (!plan) return fail(MUON_ERR_INVALID, "NULL plan");
+  if (n_iters < 0 || n_iters > MUON_MAX_NS_STEPS) return fail(MUON_ERR_INVALID, "n_iters must be in [0, 16]");
+  if (n_iters > 0 && !coeffs) return fail(MUON_ERR_INVALID, "NULL coefficients");
+  for (int i = 0; i < 3 * n_iters; ++i)
+    if (!std::isfinite(coeffs[i])) return fail(MUON_ERR_INVALID, "coefficient %d is not finite", i);
+  plan->ns_sched.assign(coeffs ? coeffs : nullptr, coeffs ? coeffs + 3 * n_iters : nullptr);
   return MUON_OK;
 }
 

@@ -160,3 +160,32 @@ def test_status_strings(nsm):
 def test_synth_library_loads(nsm):
     lib = ctypes.CDLL(os.path.join(ROOT, "synth", "libmuonsynth.so"))
     assert hasattr(lib, "synth_fill_normal") and hasattr(lib, "synth_philox")
+
+
+def test_minimax_schedule_agrees_with_the_oracle(nsm):
+    # two constructions written apart (closed-form critical points here, a dense
+    # grid in the oracle) agree to the fp32 rounding of the coefficients
+    import oracle
+    for lower, safety in ((1e-3, 1.0), (1e-2, 1.0), (1e-3, 1.02)):
+        co, err = nsm.muon_polar_express_coefficients(7, lower, safety)
+        oco, oerr = oracle.polar_express_schedule(7, lower, safety)
+        for k in range(7):
+            assert co[k] == pytest.approx(oco[k], rel=2e-6, abs=1e-6), (lower, safety, k)
+            assert err[k] == pytest.approx(oerr[k], rel=1e-5, abs=1e-12), (lower, safety, k)
+
+
+def test_schedule_arguments_are_checked(nsm):
+    out = (ctypes.c_float * 48)()
+    for n, lo, sf in ((0, 1e-3, 1.0), (17, 1e-3, 1.0), (3, 0.0, 1.0), (3, 1.0, 1.0), (3, 1e-3, 0.9),
+                      (3, 1e-3, 2.5), (3, float("nan"), 1.0)):
+        assert nsm.lib.muon_polar_express_coefficients(n, lo, sf, out, None) == nsm.MUON_ERR_INVALID, (n, lo, sf)
+    assert nsm.lib.muon_polar_express_coefficients(3, 1e-3, 1.0, None, None) == nsm.MUON_ERR_INVALID
+    p = nsm.muon_plan([(8, 16)])
+    nsm.muon_set_ns_schedule(p, [(3.0, -3.0, 1.0)] * 16)
+    nsm.muon_set_ns_schedule(p, [])
+    for bad in ([(1.0, 2.0, 3.0)] * 17, [(1.0, float("inf"), 0.0)], [(float("nan"), 0.0, 0.0)]):
+        with pytest.raises(nsm.MuonError) as e:
+            nsm.muon_set_ns_schedule(p, bad)
+        assert e.value.status == nsm.MUON_ERR_INVALID
+    assert nsm.lib.muon_set_ns_schedule(None, out, 1) == nsm.MUON_ERR_INVALID
+    assert nsm.lib.muon_set_ns_schedule(p.handle, None, 2) == nsm.MUON_ERR_INVALID
