@@ -39,6 +39,14 @@ def f32(x):
     return float(np.float32(x))
 
 
+def f32_coeffs(coeffs):
+    """One (a, b, c) or a per-iteration list of them, as the fp32 values the GPU uses."""
+    flat = list(coeffs)
+    if flat and isinstance(flat[0], (tuple, list, np.ndarray)):
+        return [tuple(f32(v) for v in t) for t in flat]
+    return tuple(f32(v) for v in flat)
+
+
 def oracle_constants(mu: float, form: str):
     """mu and (1 - mu) exactly as the kernels use them (fp32 values)."""
     mu32 = np.float32(mu)
@@ -111,7 +119,7 @@ def check_step(wl: Workload, W_prev, M_prev, W_new, M_new, *, lr, mu, nesterov, 
     what it produced.  Returns the worst (ulp, rel) seen; asserts the tolerances.
     """
     mu32, omu = oracle_constants(mu, form)
-    c32 = tuple(f32(v) for v in coeffs)
+    c32 = f32_coeffs(coeffs)
     worst_ulp, worst_rel = 0, 0.0
     for i, (r, c, k) in enumerate(wl.shapes):
         idx = range(k) if sample is None else sample(i, k)
@@ -146,8 +154,11 @@ def bf16_weight_check(W_new_bits, Wo, Wp, tol):
 
 
 def run_steps(m, wl, *, lr=0.02, mu=0.95, nesterov=True, wd=0.0, ns_steps=5, cap=512 << 20, cfg=None,
-              steps=1, form="ema", coeffs=oracle.DEFAULT_COEFFS, sample=None, tol=TOL_BF16):
-    """Run `steps` GPU Muon steps on a Workload, checking each against the oracle."""
+              steps=1, form="ema", coeffs=oracle.DEFAULT_COEFFS, sample=None, tol=TOL_BF16,
+              schedule=None):
+    """Run `steps` GPU Muon steps on a Workload, checking each against the oracle.
+    ``schedule``: per-iteration (a, b, c) set on the plan (and used by the oracle)
+    in place of ``coeffs``."""
     import torch
     cfg = cfg or m.muon_config_default()
     cfg.grad_dtype = wl.g_dtype
@@ -156,6 +167,9 @@ def run_steps(m, wl, *, lr=0.02, mu=0.95, nesterov=True, wd=0.0, ns_steps=5, cap
     cfg.ns_a, cfg.ns_b, cfg.ns_c = coeffs
     plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=cfg)
     m.allocate_workspace(plan)
+    if schedule is not None:
+        m.muon_set_ns_schedule(plan, schedule)
+        coeffs = schedule
     worst = (0, 0.0)
     for step in range(steps):
         if step > 0:
