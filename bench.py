@@ -34,19 +34,24 @@ WORKLOAD = ("qwen3-4b-layer: q 4096x2560, k/v 1024x2560, o 2560x4096, gate/up 97
             "down 2560x9728; G bf16 N(0,1e-3), M and W fp32 N(0,0.02); mu 0.95 Nesterov, lr 0.02, "
             "wd 0, 5 NS iterations (3.4445, -4.7750, 2.0315)")
 LR, MU, WD, NS_STEPS = 0.02, 0.95, 0.0, 5
+# Newton-Schulz coefficients: "fixed" (the configuration's (a, b, c) every
+# iteration) or "minimax" (per-iteration schedule, see --ns-schedule); set by main()
+NS_SCHEDULE = {"kind": "fixed", "lower": 1e-3, "safety": 1.05}
 G_SIGMA, W_SIGMA, M_SIGMA = 1e-3, 0.02, 0.02
 
 
-def ns_flops(rows, cols, steps=NS_STEPS):
+def ns_flops(rows, cols, steps=None):
     """(nominal, algorithmic) Newton-Schulz flops of one rows x cols matrix."""
+    steps = NS_STEPS if steps is None else steps
     m, n = min(rows, cols), max(rows, cols)
     nominal = steps * (4 * m * m * n + 2 * m ** 3)
     algorithmic = steps * (m * (m + 1) * n + 2 * m ** 3 + 2 * m * m * n)
     return nominal, algorithmic
 
 
-def ns_executed_flops(rows, cols, steps=NS_STEPS, bm=128, bn=256, bk=64):
+def ns_executed_flops(rows, cols, steps=None, bm=128, bn=256, bk=64):
     """Flops the tensor cores execute: whole 128x256 tiles, k rounded up to 64."""
+    steps = NS_STEPS if steps is None else steps
     m, n = min(rows, cols), max(rows, cols)
     cd = lambda a, b: -(-a // b)
     sym = sum(min(cd(m, bm), (bj * bn + bn - 1) // bm + 1) for bj in range(cd(m, bn)))
@@ -114,10 +119,30 @@ def oracle_sample(spec, n_sample):
     return out
 
 
+def oracle_coeffs():
+    """The oracle's coefficients for the configured schedule."""
+    import oracle
+    if NS_SCHEDULE["kind"] == "minimax":
+        return oracle.polar_express_schedule(NS_STEPS, NS_SCHEDULE["lower"], NS_SCHEDULE["safety"])[0]
+    return oracle.DEFAULT_COEFFS
+
+
 def oracle_step(sample):
     import oracle
+    co = oracle_coeffs()
     for W, M, G in sample:
-        oracle.muon_matrix_step(W, M, G, LR, MU, True, WD, NS_STEPS)
+        oracle.muon_matrix_step(W, M, G, LR, MU, True, WD, NS_STEPS, co)
+
+
+def set_schedule(nsm, plan):
+    """Applies --ns-schedule to a plan; returns its description for the JSON line."""
+    if NS_SCHEDULE["kind"] != "minimax":
+        return {"kind": "fixed", "coeffs": [3.4445, -4.7750, 2.0315]}
+    co, err = nsm.muon_polar_express_coefficients(NS_STEPS, NS_SCHEDULE["lower"], NS_SCHEDULE["safety"])
+    nsm.muon_set_ns_schedule(plan, co)
+    return {"kind": "minimax (per-iteration odd quintic closest to 1 on the singular-value interval)",
+            "lower": NS_SCHEDULE["lower"], "safety": NS_SCHEDULE["safety"],
+            "coeffs": [[round(v, 6) for v in t] for t in co], "worst_case_error_after_each": err}
 
 
 # matrices the CPU leg times per workload: the whole layer, or a bounded sample
@@ -342,6 +367,7 @@ def run_gpu(args):
     plan = nsm.muon_plan(shapes, bucket_cap_bytes=spec["cap"], config=cfg)
     info = nsm.muon_get_plan_info(plan)
     ws = nsm.allocate_workspace(plan)
+    schedule = set_schedule(nsm, plan)
     tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16}
     W, M, G = [], [], []
     for i, (r, c, k) in enumerate(tensors):
@@ -482,6 +508,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32x3" if tf32 else "bf16", "data": "synthetic",
         "config": {"workload": spec["desc"], "matrices_per_step": n_mats, "elements_per_step": elems,
+                   "ns_steps": NS_STEPS, "ns_schedule": schedule,
                    "buckets": int(info.n_buckets), "parallelism": f"replicas{world}",
                    "l2": f"inputs {step_bytes / 1e9:.2f} GB per step vs the 129 MB L2"},
         "ns_tflops": {"nominal": nominal / (ms * 1e-3) / 1e12, "algorithmic_in_ns_phase": ns_alg_tflops,
@@ -562,6 +589,7 @@ def run_offload(args):
     plan = nsm.muon_plan(shapes, bucket_cap_bytes=128 << 20, config=cfg)
     info = nsm.muon_get_plan_info(plan)
     ws = nsm.allocate_workspace(plan)
+    schedule = set_schedule(nsm, plan)
     hG, hM, hU = [], [], []
     for i, (r, c) in enumerate(shapes):
         g = torch.empty((r, c), dtype=torch.bfloat16, device="cuda")
@@ -597,7 +625,8 @@ def run_offload(args):
                                    "host memory; 128 MiB buckets, three staging slots (upload, compute and "
                                    "writeback of three buckets overlap); host-blocking step (drained before "
                                    "return)",
-                       "buckets": int(info.n_buckets), "matrices_per_step": len(shapes)},
+                       "buckets": int(info.n_buckets), "matrices_per_step": len(shapes),
+                       "ns_steps": NS_STEPS, "ns_schedule": schedule},
             "host_link": {"h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
                           "h2d_gbs_avg_over_step": hb / (s_ms * 1e-3) / 1e9,
                           "d2h_gbs_avg_over_step": db / (s_ms * 1e-3) / 1e9,
@@ -633,7 +662,15 @@ def main():
                     help="Newton-Schulz arithmetic: bf16 (default) or the 3xTF32 accuracy mode")
     ap.add_argument("--layers", type=int, default=None,
                     help="heads / experts: fewer layers than the full workload (profiling captures)")
+    ap.add_argument("--ns-steps", type=int, default=5, help="Newton-Schulz iterations per step (default 5)")
+    ap.add_argument("--ns-schedule", choices=["fixed", "minimax"], default="fixed",
+                    help="fixed (3.4445, -4.7750, 2.0315) every iteration, or the per-iteration minimax schedule")
+    ap.add_argument("--ns-lower", type=float, default=1e-3, help="minimax: assumed lower end of the singular values")
+    ap.add_argument("--ns-safety", type=float, default=1.05, help="minimax: widening of each fitted interval's top")
     args = ap.parse_args()
+    global NS_STEPS
+    NS_STEPS = args.ns_steps
+    NS_SCHEDULE.update(kind=args.ns_schedule, lower=args.ns_lower, safety=args.ns_safety)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
