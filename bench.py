@@ -585,7 +585,8 @@ def run_offload(args):
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     shapes = [(r, c) for _ in range(36) for _, r, c in QWEN3_4B_LAYER]
-    cfg = nsm.muon_config_default(offload=1, max_inflight=2, timing=1)
+    zero_copy = args.offload_mode == "zerocopy"
+    cfg = nsm.muon_config_default(offload=1, max_inflight=2, timing=1, offload_zero_copy=1 if zero_copy else 0)
     plan = nsm.muon_plan(shapes, bucket_cap_bytes=128 << 20, config=cfg)
     info = nsm.muon_get_plan_info(plan)
     ws = nsm.allocate_workspace(plan)
@@ -626,7 +627,9 @@ def run_offload(args):
                                    "writeback of three buckets overlap); host-blocking step (drained before "
                                    "return)",
                        "buckets": int(info.n_buckets), "matrices_per_step": len(shapes),
-                       "ns_steps": NS_STEPS, "ns_schedule": schedule},
+                       "ns_steps": NS_STEPS, "ns_schedule": schedule,
+                       "offload_mode": "zero-copy (kernels read and write the pinned host buffers)" if zero_copy
+                       else "staged (copy engines into device slots)"},
             "host_link": {"h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
                           "h2d_gbs_avg_over_step": hb / (s_ms * 1e-3) / 1e9,
                           "d2h_gbs_avg_over_step": db / (s_ms * 1e-3) / 1e9,
@@ -662,6 +665,8 @@ def main():
                     help="Newton-Schulz arithmetic: bf16 (default) or the 3xTF32 accuracy mode")
     ap.add_argument("--layers", type=int, default=None,
                     help="heads / experts: fewer layers than the full workload (profiling captures)")
+    ap.add_argument("--offload-mode", choices=["copy", "zerocopy"], default="copy",
+                    help="offload workload: staged copies (default) or zero-copy kernel access to host memory")
     ap.add_argument("--ns-steps", type=int, default=5, help="Newton-Schulz iterations per step (default 5)")
     ap.add_argument("--ns-schedule", choices=["fixed", "minimax"], default="fixed",
                     help="fixed (3.4445, -4.7750, 2.0315) every iteration, or the per-iteration minimax schedule")

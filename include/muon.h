@@ -103,7 +103,12 @@ typedef struct {
   int32_t timing;           /* 1: record per-bucket CUDA events for muon_get_stats */
   int32_t offload;          /* 1: reserve host-link staging slots for muon_offload_step */
   int32_t ns_kernel;        /* MUON_NS_KERNEL_AUTO or MUON_NS_KERNEL_GEMM */
-  int32_t reserved[3];
+  int32_t offload_zero_copy; /* with offload = 1: 1 makes muon_offload_step's kernels read G and
+                                M and write M and U' in the pinned host buffers themselves
+                                (mapped into the device's address space; no staging slots,
+                                no copy engines, everything on the compute stream); 0 stages
+                                each bucket through device slots with copy-engine copies */
+  int32_t reserved[2];
 } muon_config;
 
 /* Fills *cfg with (3.4445, -4.7750, 2.0315), eps 1e-7, bf16 NS, EMA momentum,

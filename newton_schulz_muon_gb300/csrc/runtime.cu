@@ -406,7 +406,7 @@ muon_status build_plan(muon_plan_t* p, const muon_shape* shapes, int32_t n, cons
     }
   p->off_sched = off; off = align_up(off + sched, kAlign);
   p->sched_bytes = sched;
-  if (p->cfg.offload) {
+  if (p->cfg.offload && !p->cfg.offload_zero_copy) {
     p->n_slots = std::max(1, std::min(2, (int)p->cfg.max_inflight)) + 1;
     p->slot_bytes = align_up((size_t)p->max_elems * grad_size(p->cfg), kAlign) +
                     2 * align_up((size_t)p->max_elems * 4, kAlign);
@@ -562,7 +562,6 @@ void ns_coeffs(const muon_plan_t* p, int k, float out[3]) {
 
 muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st,
                              const ApplyArgs& fused) {
-  const muon_config& c = p->cfg;
   SmallArgs sa;
   std::memset(&sa, 0, sizeof(sa));
   std::vector<size_t> order(b.groups.size());
@@ -976,12 +975,107 @@ muon_status muon_step(muon_plan_t* p, void* const* params, const void* const* gr
   return MUON_OK;
 }
 
+namespace {
+
+// The device address of pinned host memory (the same address under unified
+// addressing when the allocation is mapped, as cudaHostAlloc memory is).
+muon_status mapped(const void* host, const char* what, int i, const void** dev) {
+  void* d = nullptr;
+  cudaError_t e = cudaHostGetDevicePointer(&d, const_cast<void*>(host), 0);
+  if (e != cudaSuccess || d == nullptr) {
+    cudaGetLastError();
+    return fail(MUON_ERR_NOT_PINNED, "%s[%d] is pinned but not mapped into the device's address space", what, i);
+  }
+  *dev = d;
+  return MUON_OK;
+}
+
+// Zero-copy offload: per bucket, the momentum kernel reads G and M from host
+// memory over the host link and writes M back there, Newton-Schulz runs on the
+// device, and the last UPDATE's epilogue writes U' into the host buffer; all on
+// the compute stream, drained before returning.
+muon_status offload_zero_copy(muon_plan_t* p, const void* const* h_grads, void* const* h_momentum,
+                              void* const* h_update_out, float mu, int32_t nesterov, int32_t ns_steps,
+                              cudaStream_t cs, int64_t timeout_ms) {
+  const size_t gs = grad_size(p->cfg);
+  const bool timing = p->cfg.timing != 0;
+  const int n = (int)p->tensors.size();
+  std::vector<const void*> dg(n), dm(n), du(n);
+  for (int i = 0; i < n; ++i) {
+    muon_status s;
+    if ((s = mapped(h_grads[i], "h_grads", i, &dg[i])) != MUON_OK) return s;
+    if ((s = mapped(h_momentum[i], "h_momentum", i, &dm[i])) != MUON_OK) return s;
+    if ((s = mapped(h_update_out[i], "h_update_out", i, &du[i])) != MUON_OK) return s;
+  }
+  int64_t h2d_bytes = 0, d2h_bytes = 0;
+  cudaError_t e;
+  if (timing) cudaEventRecord(p->step_start, cs);
+  for (size_t bi = 0; bi < p->buckets.size(); ++bi) {
+    const Bucket& b = p->buckets[bi];
+    auto ptrs = [&](const Run& r) {
+      const TensorInfo& t = p->tensors[r.tensor];
+      RunPtrs rp;
+      rp.g = static_cast<const uint8_t*>(dg[r.tensor]) + (size_t)r.first * t.stride * gs;
+      rp.m = const_cast<float*>(static_cast<const float*>(dm[r.tensor])) + (size_t)r.first * t.stride;
+      rp.w = const_cast<float*>(static_cast<const float*>(du[r.tensor])) + (size_t)r.first * t.stride;
+      rp.stride = t.stride;
+      return rp;
+    };
+    for (const BGroup& g : b.groups)
+      for (const Run& r : g.runs) {
+        const TensorInfo& t = p->tensors[r.tensor];
+        h2d_bytes += r.count * t.rows * t.cols * (int64_t)(gs + 4);
+        d2h_bytes += r.count * t.rows * t.cols * 8;
+      }
+    if (timing) {
+      cudaEventRecord(p->events[bi].start, cs);
+      cudaEventRecord(p->events[bi].prep, cs);
+    }
+    PrepArgs pa;
+    make_prep_args(p, b, ptrs, mu, nesterov, pa);
+    if ((e = launch_prep(pa, cs)) != cudaSuccess) return cuda_fail(e, "momentum_prep launch");
+    if ((e = launch_norm(pa, cs)) != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
+    if (timing) cudaEventRecord(p->events[bi].h2d, cs);
+    ApplyArgs aa;
+    make_apply_args(p, b, ptrs, ns_steps & 1, 0.f, 0.f, 1, ns_steps, aa);
+    muon_status s = enqueue_ns(p, b, ns_steps, cs, ns_steps > 0 ? &aa : nullptr);
+    if (s != MUON_OK) return s;
+    if (timing) cudaEventRecord(p->events[bi].ns, cs);
+    if (ns_steps == 0 && (e = launch_apply(aa, cs)) != cudaSuccess) return cuda_fail(e, "emit launch");
+    if (timing) {
+      cudaEventRecord(p->events[bi].apply, cs);
+      cudaEventRecord(p->events[bi].d2h_start, cs);
+      cudaEventRecord(p->events[bi].d2h, cs);
+    }
+  }
+  if (timing) cudaEventRecord(p->step_end, cs);
+  cudaEvent_t done = p->slot_d2h[0];  // the bind step creates at least one
+  e = cudaEventRecord(done, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  // drain: the host reads the results next
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    e = cudaEventQuery(done);
+    if (e == cudaSuccess) break;
+    if (e != cudaErrorNotReady) return cuda_fail(e, "zero-copy offload step");
+    if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(timeout_ms))
+      return fail(MUON_ERR_TIMEOUT, "zero-copy offload step did not finish within %lld ms", (long long)timeout_ms);
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  p->offload_last = true;
+  p->last_h2d_bytes = h2d_bytes;
+  p->last_d2h_bytes = d2h_bytes;
+  return MUON_OK;
+}
+
+}  // namespace
+
 muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* const* h_momentum,
                               void* const* h_update_out, int64_t n_mats, float mu, int32_t nesterov,
                               int32_t ns_steps, void* compute, void* copy, int64_t timeout_ms) {
   if (!p) return fail(MUON_ERR_INVALID, "plan is NULL");
   if (!p->ws) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
-  if (!p->cfg.offload || p->n_slots < 2)
+  if (!p->cfg.offload || (!p->cfg.offload_zero_copy && p->n_slots < 2))
     return fail(MUON_ERR_NO_WORKSPACE, "plan was made without cfg.offload = 1 (no staging slots)");
   if (!h_grads || !h_momentum || !h_update_out) return fail(MUON_ERR_INVALID, "pointer array is NULL");
   if (n_mats != (int64_t)p->tensors.size())
@@ -995,6 +1089,8 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
     if ((s = check_pinned(h_update_out[i], "h_update_out", i)) != MUON_OK) return s;
   }
   cudaStream_t cs = static_cast<cudaStream_t>(compute);
+  if (p->cfg.offload_zero_copy) return offload_zero_copy(p, h_grads, h_momentum, h_update_out, mu, nesterov, ns_steps,
+                                                         cs, timeout_ms);
   cudaStream_t ds = copy ? static_cast<cudaStream_t>(copy) : p->d2h_stream;
   cudaStream_t hs = p->h2d_stream;
   const size_t gs = grad_size(p->cfg);

@@ -181,9 +181,9 @@ def _pinned(arr, dtype_code):
     return t.pin_memory()
 
 
-def _offload(m, wl, cap, inflight, ns_steps=5, mu=0.95):
+def _offload(m, wl, cap, inflight, ns_steps=5, mu=0.95, zero_copy=0):
     import torch
-    cfg = m.muon_config_default(offload=1, max_inflight=inflight, timing=1)
+    cfg = m.muon_config_default(offload=1, max_inflight=inflight, timing=1, offload_zero_copy=zero_copy)
     cfg.grad_dtype = wl.g_dtype
     plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=cfg)
     m.allocate_workspace(plan)
@@ -215,6 +215,23 @@ def test_offload_matches_oracle_and_is_order_independent(m):
     M2, U2, _, _ = _offload(m, wl, cap=400_000, inflight=2)
     for a, b in zip(M1 + U1, M2 + U2):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("shapes", [
+    [(256, 512), (300, 200, 2), (64, 640), (512, 128, 3)],   # grouped GEMM buckets
+    [(128, 1024, 4), (96, 700), (700, 96)],                  # small-matrix kernel buckets
+])
+def test_zero_copy_offload_is_bitwise_the_staged_one(m, shapes):
+    # the same kernels read and write the pinned host buffers directly instead of
+    # device staging slots: same bytes out, a smaller workspace, fewer launches of
+    # nothing but copies
+    wl = Workload(shapes, m_sigma=0.02, g_sigma=1e-3)
+    M1, U1, st1, p1 = _offload(m, wl, cap=400_000, inflight=2)
+    M2, U2, st2, p2 = _offload(m, wl, cap=400_000, inflight=2, zero_copy=1)
+    for a, b in zip(M1 + U1, M2 + U2):
+        assert np.array_equal(a, b)
+    assert st2.h2d_bytes == st1.h2d_bytes and st2.d2h_bytes == st1.d2h_bytes
+    assert m.muon_get_plan_info(p2).workspace_bytes < m.muon_get_plan_info(p1).workspace_bytes
 
 
 def test_offload_rejects_pageable_host_memory(m):
