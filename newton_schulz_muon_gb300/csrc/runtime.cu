@@ -659,7 +659,7 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
             G.ct_hi = ns + g.off_xt[nxt]; G.ct_lo = lo(g.off_xt_lo[nxt]);
             G.ct_ld = g.ld_t; G.ct_mstride = g.n * g.ld_t;
           }
-          if (!tf32) { G.map_c = g.ex[nxt]; G.map_d = g.ex[cur]; }
+          if (!tf32) G.map_c = g.ex[nxt];
           G.c_hi = ns + g.off_x[nxt]; G.c_lo = lo(g.off_x_lo[nxt]);
           G.d_hi = ns + g.off_x[cur]; G.d_lo = lo(g.off_x_lo[cur]);
           G.c_ld = g.ld_n; G.c_mstride = g.m * g.ld_n;
