@@ -203,6 +203,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream (launched
+// with programmatic stream serialisation) be scheduled as this grid's CTAs exit,
+// and wait until the grids this one depends on have completed, their writes
+// visible.  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -398,6 +398,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
   __syncthreads();
   if constexpr (kCL > 1) cluster_sync();  // barriers of both CTAs exist before any remote signal
   tc_fence_after();
+  // The prologue above overlaps the previous launch's last tiles; its outputs (X,
+  // A, B', the norm scales) are read only after it has completed.
+  griddep_launch_dependents();
+  griddep_wait();
   const uint32_t tmem_base = tmem_slot;
   const int mode = a.mode;
   const bool mn_b = (mode == kUpdate) && !kTF32;  // B operand read MN-major
@@ -856,18 +860,23 @@ cudaError_t launch_impl(const GemmArgs& a, int num_sms, cudaStream_t s) {
   if (a.n_clusters <= 0 || a.n_clusters > maxc) return cudaErrorInvalidValue;
   auto kernel = ns_gemm_kernel<kTF32, kCL>;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(a.n_clusters * kCL);
   cfg.blockDim = dim3(kThreadsG);
   cfg.dynamicSmemBytes = Cfg<kTF32, kCL>::kSmem;
   cfg.stream = s;
+  // may start as the previous kernel of the stream drains (the kernel waits for it
+  // with griddepcontrol.wait before reading anything it wrote)
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (kCL > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kCL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
