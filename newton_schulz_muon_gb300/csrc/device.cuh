@@ -53,11 +53,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// `count` arrivals at once.
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
 // 4-byte asynchronous copy global -> shared (no register staging); completion
 // is tracked per thread with cp.async groups.
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {

@@ -4,16 +4,20 @@
 // The iteration is the one of the grouped GEMM kernel (DeepSpeed issue "[RFC]
 // Enable Correct and High-Performance Muon Optimizer under ZeRO CPU Offload",
 // section 2; "Muon Optimizer + FSDP", section 背景):
-//   A = X X^T,  B = b A + c A A,  X' = a X + B X.
+//   A = X X^T,  B' = a I + b A + c A A,  X' = B' X
+// (X' = a X + (b A + c A A) X with the a X term carried by B', as the grouped
+// kernel does in bf16: near convergence B' has eigenvalues near 1 where b A + c A A
+// has them near a - 1, so rounding B' to bf16 loses less, and the UPDATE
+// epilogue reads no X).
 // The matrices this kernel exists for are the per-head slices of a fused QKV
 // projection (128 rows each; DeepSpeed issue #8463, section 4.D).  At m = 128 the
 // three GEMMs of one iteration do ~3 flops per byte of X, so a launch per GEMM
 // streams X, A and B through HBM every iteration.  Here A and B never leave the
 // SM, and X is read once and written once per iteration:
 //
-//   * A and B (128 x 128 bf16, 32 KB) live in shared memory in the tcgen05
-//     128-byte-swizzled K-major layout; B overwrites A in place (each epilogue
-//     thread reads its A elements before writing the same B elements, after the
+//   * A and B' (128 x 128 bf16, 32 KB) live in shared memory in the tcgen05
+//     128-byte-swizzled K-major layout; B' overwrites A in place (each epilogue
+//     thread reads its A elements before writing the same B' elements, after the
 //     A A product has completed).
 //   * X is streamed in 128-column chunks (two 128-row x 64-column boxes) through
 //     a TMA ring.  The same boxes serve both uses: K-major operand of the Gram,
@@ -48,7 +52,8 @@
 //              Gram 128 columns and three UPDATE buffers of 128, the first of
 //              which also takes A A).  Within an UPDATE it issues whichever is
 //              ready next: the UPDATE of the next chunk (a ring stage and an
-//              accumulator free) or the fused Gram of the next X' tile.
+//              accumulator free; its commit releases the stage) or the fused
+//              Gram of the next X' tile.
 //   warps 2-17 epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (rows), the four
 //              warps of a lane quadrant split the columns (32 each).  Four
 //              warps per SM sub-partition hide the latency of the accumulator
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t full_bar[kStagesS];
-  __shared__ __align__(8) uint64_t empty_bar[kStagesS];  // 8 arrivals: the epilogue warps, or the MMA issuer
+  __shared__ __align__(8) uint64_t empty_bar[kStagesS];  // the MMA issuer's commit: its MMAs have read the stage
   __shared__ __align__(8) uint64_t gram_full;            // Gram accumulated (MMA commit)
   __shared__ __align__(8) uint64_t a_ready;              // A in shared memory (epilogue warps)
   __shared__ __align__(8) uint64_t poly_full;            // A A accumulated (MMA commit)
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesS; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kEpiWarps);
+      mbar_init(&empty_bar[s], 1);
     }
     mbar_init(&gram_full, 1);
     mbar_init(&a_ready, kEpiWarps);
@@ -492,7 +497,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
       const SmallGroup& G = a.g[t.g];
       const int nch = (G.n + kChunkCols - 1) / kChunkCols;
       // Gram of iteration 0 over X0 chunks from the ring; the commit releases
-      // the stage (its arrival plus the others given now make the epilogue's)
+      // the stage
       for (int j = 0; j < nch; ++j) {
         const bool got = mbar_wait(&full_bar[stage], phase, abort_p, status);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
@@ -500,7 +505,6 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         if (lane == 0) {
           gram_tile(smem_u32(ring + (size_t)stage * kChunk), j == 0);
           mma_commit<1>(&empty_bar[stage]);
-          mbar_arrive_cnt(&empty_bar[stage], kEpiWarps - 1);
         }
         __syncwarp();
         ring_advance(stage, phase, 1);
@@ -549,11 +553,12 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
                                 kk != 0 ? 1u : 0u);
                 }
                 mma_commit<1>(&u_full[ub]);
+                mma_commit<1>(&empty_bar[stage]);  // free once these MMAs have read it
               }
               __syncwarp();
               ++uc;
               ++jn;
-              ring_advance(stage, phase, 1);  // the epilogue releases the stage
+              ring_advance(stage, phase, 1);
               progressed = true;
             }
           }
@@ -618,8 +623,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
     const int p0 = (part & 1) * 4;
     uint8_t* ab = smem + kOffAB + (size_t)box * kTile;    // this warp's box of A / B
     float* wbuf = reinterpret_cast<float*>(smem + kOffXS + (size_t)ew * kWarpBuf);
-    int stage = 0;
-    uint32_t phase = 0, gp = 0, pp = 0, uc = 0, xc = 0;
+    uint32_t gp = 0, pp = 0, uc = 0, xc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
       const UnitRef t = decode_unit(a, u);
@@ -627,7 +631,6 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
       const int nch = (G.n + kChunkCols - 1) / kChunkCols;
       const int mat = G.mat_base + t.b;
       const float s = a.scale[mat];
-      ring_advance(stage, phase, nch);  // the Gram's X0 chunks are released by the MMA issuer
       for (int k = 0; ok && k < K; ++k) {
         // ---- A = (s^2 in iteration 0) X X^T, bf16, into shared memory ----
         ok = __all_sync(0xffffffffu, mbar_wait(&gram_full, gp, abort_p, status));
@@ -650,7 +653,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_ready);
-        // ---- B = b A + c (A A), in place over A ----
+        // ---- B' = a I + b A + c (A A), in place over A ----
         ok = __all_sync(0xffffffffu, mbar_wait(&poly_full, pp, abort_p, status));
         pp ^= 1u;
         if (!ok) break;
@@ -664,7 +667,10 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
             float x[8], w[8];
             unpack8(*p, x);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = a.coef[k][2] * v[8 * q + e] + a.coef[k][1] * x[e];
+            for (int e = 0; e < 8; ++e) {
+              w[e] = a.coef[k][2] * v[8 * q + e] + a.coef[k][1] * x[e];
+              if (quad == part && 8 * q + e == lane) w[e] += a.coef[k][0];  // the diagonal (r, r)
+            }
             *p = pack8(w);
           }
         }
@@ -672,10 +678,9 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&b_ready);
-        // ---- X' = (s in iteration 0) (B X + a X), chunk by chunk ----
+        // ---- X' = (s in iteration 0) B' X, chunk by chunk ----
         const bool last = k + 1 == K;
         const float alpha = k == 0 ? s : 1.f;
-        const float beta = a.coef[k][0] * alpha;
         ApplyTarget tg{};
         bool vec = false;
         if (last) {
@@ -693,7 +698,6 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
             cp_async_commit();
           }
           ok = mbar_wait(&u_full[ub], (uc / kUBufs) & 1u, abort_p, status) &&
-               mbar_wait(&full_bar[stage], phase, abort_p, status) &&
                (last || mbar_wait(&xs_empty[xb], ((xc / kXsBufs) & 1u) ^ 1u, abort_p, status));
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
@@ -706,28 +710,13 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
           tc_fence_after();
           float v[32];
           tmem_ld_32x32b_x32(tmem + lane_base + kColU + 128u * (uint32_t)ub + (uint32_t)(part * 32), v);
-          const uint8_t* xsrc = ring + (size_t)stage * kChunk + (size_t)box * kTile;
-          uint4 xr[4];
+          if (k == 0) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) xr[q] = *reinterpret_cast<const uint4*>(xsrc + sw128(r, p0 + q));
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float x[8];
-            unpack8(xr[q], x);
-            if (k == 0) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v[8 * q + e] = alpha * v[8 * q + e] + beta * x[e];
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v[8 * q + e] = __fmaf_rn(beta, x[e], v[8 * q + e]);
-            }
+            for (int e = 0; e < 32; ++e) v[e] *= alpha;
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&empty_bar[stage]);
-            mbar_arrive(&u_empty[ub]);
-          }
+          if (lane == 0) mbar_arrive(&u_empty[ub]);
           if (last) {
             cp_async_wait<0>();
             __syncwarp();
@@ -745,7 +734,6 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
             ++xc;
           }
           ++uc;
-          ring_advance(stage, phase, 1);
         }
         if (last) cp_async_wait<0>();
       }
