@@ -22,7 +22,9 @@
 //   * X is streamed in 128-column chunks (two 128-row x 64-column boxes) through
 //     a TMA ring.  The same boxes serve both uses: K-major operand of the Gram,
 //     MN-major B operand of the UPDATE (k = the 128 rows).  Rows >= m and columns
-//     >= n are zero-filled by TMA, so padding contributes nothing.  Every MMA has
+//     >= n are zero-filled by TMA, so padding contributes nothing.  Successive
+//     passes over X alternate direction, so a pass begins on the chunks the
+//     previous one wrote last (still in L2 more often).  Every MMA has
 //     N = 128: on one SM a tcgen05.mma of M = 128 takes at least ~60 cycles
 //     whatever its N, so narrower products would idle the tensor pipe.
 //   * The Gram of iteration k+1 is fused into the UPDATE of iteration k: the
@@ -398,11 +400,15 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
       const SmallGroup& G = a.g[t.g];
       const int nch = (G.n + kChunkCols - 1) / kChunkCols;
       for (int pass = 0; ok && pass <= K; ++pass) {
+        // serpentine order: odd passes walk the chunks backwards, starting with
+        // those the previous pass wrote last, the likeliest to be still in L2
+        const bool rev = pass & 1;
+        auto chunk = [&](int j) { return rev ? nch - 1 - j : j; };
         if (pass == 0 || pass == K) {  // no X' to store: plain loads
           for (int j = 0; j < nch; ++j) {
             const bool got = mbar_wait(&empty_bar[stage], phase ^ 1u, abort_p, status);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-            load_chunk(G, t.b, j);
+            load_chunk(G, t.b, chunk(j));
           }
           continue;
         }
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         while (jl < nch || js < nch) {
           bool progressed = false;
           if (jl < nch && poll(&empty_bar[stage], phase ^ 1u)) {
-            load_chunk(G, t.b, jl);
+            load_chunk(G, t.b, chunk(jl));
             ++jl;
             progressed = true;
           }
@@ -419,9 +425,9 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
           if (js < jl && poll(&xs_full[xb], (xc / kXsBufs) & 1u)) {
             if (lane == 0) {
               const uint8_t* src = smem + kOffXS + (size_t)xb * kChunk;
-              tma_store_3d_hint(&G.map_x, src, js * kChunkCols, 0, t.b, keep);
-              if (js * kChunkCols + kBoxCols < G.n)
-                tma_store_3d_hint(&G.map_x, src + kTile, js * kChunkCols + kBoxCols, 0, t.b, keep);
+              const int cs = chunk(js) * kChunkCols;
+              tma_store_3d_hint(&G.map_x, src, cs, 0, t.b, keep);
+              if (cs + kBoxCols < G.n) tma_store_3d_hint(&G.map_x, src + kTile, cs + kBoxCols, 0, t.b, keep);
               bulk_commit_group();
               if (js > 0) {  // the previous tile's store has read it: its store half of "free"
                 bulk_wait_group_read<1>();
@@ -690,7 +696,9 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         for (int j = 0; j < nch; ++j) {
           const int ub = (int)(uc % kUBufs);
           const int xb = (int)(xc % kXsBufs);
-          const int64_t c0 = (int64_t)j * kChunkCols + part * 32;  // this warp's 32 columns
+          // UPDATE k is the producer's pass k + 1: backwards when k is even
+          const int jc = (k & 1) ? j : nch - 1 - j;
+          const int64_t c0 = (int64_t)jc * kChunkCols + part * 32;  // this warp's 32 columns
           if (last && j > 0) {
             // the weights of this warp's piece load while the chunk's accumulator
             // is awaited and drained (the buffer's previous piece is stored)
