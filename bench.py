@@ -167,31 +167,60 @@ def cpu_baseline_leg(name, min_seconds=3.0):
             "sample": f"{what}, {reps} pass(es), {dt:.1f} s; numpy fp64 with OpenBLAS threads"}
 
 
+# seconds of oracle work the reference arm's timed steps may take in total
+REF_TIMED_BUDGET_S = 120.0
+
+
 def run_reference(args):
-    """The oracle, as it stands, on the host cores: the reference arm of this bench."""
+    """The oracle, as it stands, on the host cores: the reference arm of this bench.
+
+    Each timed step runs the oracle on a sample of the workload's matrices, the
+    cheapest first, as many as fit in REF_TIMED_BUDGET_S / steps at the rate the
+    warm-up measured (at least one), so the run ends in a few minutes for any
+    --steps.  The fp64 flop rate of those steps, divided into the workload's
+    Newton-Schulz flops, gives the workload's matrices/s.
+    """
     rank, world, _ = dist_env()
     if rank != 0:
         return
     name = args.workload
     spec = workload_spec("layer" if name == "offload" else name)
     sample = oracle_sample(spec, CPU_SAMPLE[name])
-    for _ in range(args.warmup):            # warm-up on the first sampled matrix only
-        oracle_step(sample[:1])
+    flops = [ns_flops(*W.shape)[1] for (W, _, _) in sample]
+    order = sorted(range(len(sample)), key=lambda i: flops[i])
+    t0 = time.perf_counter()
+    for _ in range(args.warmup):            # warm-up on the cheapest sampled matrix
+        oracle_step([sample[order[0]]])
+    rate = max(args.warmup, 1) * flops[order[0]] / max(time.perf_counter() - t0, 1e-9)
+    per_step = max(0.5, REF_TIMED_BUDGET_S / max(args.steps, 1))
+    picked, est = [], 0.0
+    for i in order:
+        if picked and est + flops[i] / rate > per_step:
+            break
+        picked.append(i)
+        est += flops[i] / rate
+    timed = [sample[i] for i in picked]
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(sample)
+        oracle_step(timed)
     dt = time.perf_counter() - t0
-    value = args.steps * len(sample) / dt
+    measured = args.steps * sum(flops[i] for i in picked) / dt          # fp64 flop/s of the oracle
+    work = [(r, c) for (r, c, k) in spec["tensors"] for _ in range(k)]
+    step_s = sum(ns_flops(r, c)[1] for r, c in work) / measured          # one whole workload step
+    value = len(work) / step_s
+    sample_desc = (f"each timed step runs the oracle on {len(timed)} of the workload's matrices "
+                   f"(the cheapest of an evenly spaced sample of {len(sample)}, {per_step:.1f} s per step at "
+                   f"most); matrices/s of the whole workload from the measured fp64 flop rate "
+                   f"({measured / 1e9:.2f} GFLOP/s of Newton-Schulz work), extrapolated by flop ratio")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * step_s,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": spec["desc"] if name != "offload" else name,
-                                        "matrices_per_step": len(sample)},
+                                        "matrices_per_step": len(work), "ns_steps": NS_STEPS,
+                                        "timed_sample_ms_per_step": 1000 * dt / args.steps},
         "cpu_baseline": {"value": value, "unit": "matrices/s", "cores": cores_used(), "kind": "oracle",
-                         "sample": f"each timed step runs the oracle on {len(sample)} matrices of the workload "
-                                   f"({'all' if name in ('layer', 'offload') else 'evenly spaced'}); "
-                                   "warm-up steps run the first of them only"},
+                         "sample": sample_desc},
         "e2e": {"value": value, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
