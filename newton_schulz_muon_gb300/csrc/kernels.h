@@ -100,11 +100,6 @@ struct GemmGroup {
   CUtensorMap map_b_lo;
   CUtensorMap map_c;     // bf16 epilogue: output C, box {32, 32}, 64-byte swizzle (TMA stores)
   CUtensorMap map_d;     // bf16 epilogue: POLY's addend A, same box (TMA loads)
-  // bf16 POLY: A is stored as its upper 256-blocks; k blocks left of an
-  // operand's row block are read transposed from the stored part, MN-major boxes
-  // {64 (rows of the operand), 64 (k)}
-  CUtensorMap map_a_mn;
-  CUtensorMap map_b_mn;
   void* c_hi;            // output (bf16 or tf32-hi fp32)
   float* c_lo;           // output tf32-lo part
   const void* d_hi;      // epilogue addend (POLY: A; 3xTF32 UPDATE: X)

@@ -20,17 +20,14 @@
 // has eigenvalues near 1 where B has them near a - 1, so rounding B' to bf16 loses
 // less than rounding B, and the UPDATE epilogue reads no addend.
 //
-// Symmetric storage.  bf16 A is stored as exactly the tiles computed: the
-// 256 x 256 blocks on and above the diagonal, each written whole.  Element (i, k)
-// is held at (i, k) when i / 256 <= k / 256 and at (k, i) otherwise, so POLY reads
-// a 64-deep k block of an operand in place (K-major rows) when the block lies in
-// or right of the operand rows' 256-block, and from the transposed position
-// (MN-major, rows of the block contiguous) when it lies left of it; the tensor
-// core takes either major per instruction.  POLY writes B' whole (its tiles above
-// the diagonal blocks also as their transposes), because transposed reads of the
-// A operand slow UPDATE's mainloop more than the extra boxes cost POLY's epilogue
-// (measured on one Qwen3-4B layer and on a 169-matrix bucket of 768 x 2048).
-// 3xTF32 keeps full symmetric matrices (upper part mirrored) and K-major reads.
+// Symmetric storage.  The GRAM and POLY tiles are the 256 x 256 blocks on and
+// above the diagonal.  In bf16 a diagonal block is computed, and written, whole,
+// and a block above it also writes its transpose (one more TMA box per chunk from
+// the same staging), so A and B' are whole and every operand is read in place
+// (K-major rows).  Storing only the computed blocks and reading the blocks left of
+// an operand's rows transposed (MN-major) was measured slower: the transposed A
+// operand slows the mainloop more than the extra boxes cost the epilogue.  3xTF32
+// mirrors the strictly upper part element by element.
 //
 // In the first iteration X holds the un-normalised V; the per-matrix factor
 // s = 1/(||V||_F + eps) is applied in the epilogues (GRAM: s^2, UPDATE: s).  The
@@ -405,11 +402,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
   const uint32_t tmem_base = tmem_slot;
   const int mode = a.mode;
   const bool mn_b = (mode == kUpdate) && !kTF32;  // B operand read MN-major
-  // bf16 A holds only its 256-blocks on or above the diagonal; POLY's operands
-  // (both rows of A) read each k block that lies left of their rows' 256-block
-  // transposed, from the stored part
-  const bool sym_a = !kTF32 && mode == kPoly;
-  const bool sym_b = sym_a;
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
@@ -432,32 +424,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           if (leader) mbar_arrive_expect_tx(&full_bar[stage], C::kTx);
           const uint32_t bar = kCL > 1 ? mapa_shared(&full_bar[stage], 0) : smem_u32(&full_bar[stage]);
           const int k0 = kb * C::kBK;
-          const int i0 = tc.bi * kBM;                                  // first row of operand A
-          const int j0 = tc.bj * kBN + (kCL > 1 ? rank * C::kBRows : 0);  // first row of operand B
-          const bool a_low = sym_a && (k0 >> 8) < (i0 >> 8);
-          const bool b_low = sym_b && (k0 >> 8) < (j0 >> 8);
-          if (a_low || b_low) {
-            // transposed reads: 64-row chunks of the operand, each a {64, 64} box
-            if (a_low)
-              for (int q = 0; q < kBM / C::kBK; ++q) {
-                if constexpr (kCL == 1) tma_load_3d(sa + q * C::kChunkBytes, &G.map_a_mn, &full_bar[stage], i0 + q * C::kBK, k0, tc.b);
-                else tma_load_3d_pair(sa + q * C::kChunkBytes, &G.map_a_mn, bar, i0 + q * C::kBK, k0, tc.b);
-              }
-            if (b_low)
-              for (int q = 0; q < C::kChunks; ++q) {
-                if constexpr (kCL == 1) tma_load_3d(sb + q * C::kChunkBytes, &G.map_b_mn, &full_bar[stage], j0 + q * C::kBK, k0, tc.b);
-                else tma_load_3d_pair(sb + q * C::kChunkBytes, &G.map_b_mn, bar, j0 + q * C::kBK, k0, tc.b);
-              }
-          }
 #pragma unroll
           for (int part = 0; part < C::kParts; ++part) {
             const CUtensorMap* ma = part ? &G.map_a_lo : &G.map_a;
             const CUtensorMap* mb = part ? &G.map_b_lo : &G.map_b;
             uint8_t* sbp = sb + part * C::kB;
             if constexpr (kCL == 1) {
-              if (!a_low) tma_load_3d(sa + part * C::kA, ma, &full_bar[stage], k0, tc.bi * kBM, tc.b);
-              if (b_low) {
-              } else if (mn_b) {
+              tma_load_3d(sa + part * C::kA, ma, &full_bar[stage], k0, tc.bi * kBM, tc.b);
+              if (mn_b) {
 #pragma unroll
                 for (int q = 0; q < C::kChunks; ++q)
                   tma_load_3d(sbp + q * C::kChunkBytes, mb, &full_bar[stage], tc.bj * kBN + q * C::kBK, k0, tc.b);
@@ -468,9 +442,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
               }
             } else {
               // own 128 rows of A and own half of B, completing on the even CTA's barrier
-              if (!a_low) tma_load_3d_pair(sa + part * C::kA, ma, bar, k0, tc.bi * kBM, tc.b);
-              if (b_low) {
-              } else if (mn_b) {
+              tma_load_3d_pair(sa + part * C::kA, ma, bar, k0, tc.bi * kBM, tc.b);
+              if (mn_b) {
 #pragma unroll
                 for (int q = 0; q < C::kChunks; ++q)
                   tma_load_3d_pair(sbp + q * C::kChunkBytes, mb, bar, tc.bj * kBN + rank * C::kBRows + q * C::kBK,
@@ -518,19 +491,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           if (lane == 0) {
             const uint32_t sa = smem_u32(smem + (size_t)stage * C::kStage);
             const uint32_t sb = sa + C::kParts * C::kA;
-            // the same k-block choice as the producer's (both CTAs of a pair share
-            // the row block of A and the column block of B)
-            const int k0 = kb * C::kBK;
-            const bool a_low = sym_a && (k0 >> 8) < ((tc.bi * kBM) >> 8);
-            const bool b_low = sym_b && (k0 >> 8) < ((tc.bj * kBN) >> 8);
-            const bool b_t = mn_b || b_low;
-            const uint32_t id = make_idesc(C::kFormat, kBM * kCL, kBN, b_t ? 1u : 0u, a_low ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < C::kBK / C::kInstK; ++kk) {
-              const uint64_t ad = a_low ? smem_desc_sw128(sa + kk * C::kInstK * 128, C::kChunkBytes, 1024)
-                                        : smem_desc_sw128(sa + kk * 32, 16, 1024);
-              const uint64_t bd = b_t ? smem_desc_sw128(sb + kk * C::kInstK * 128, C::kChunkBytes, 1024)
-                                      : smem_desc_sw128(sb + kk * 32, 16, 1024);
+              const uint64_t ad = smem_desc_sw128(sa + kk * 32, 16, 1024);
+              const uint64_t bd = mn_b ? smem_desc_sw128(sb + kk * C::kInstK * 128, C::kChunkBytes, 1024)
+                                       : smem_desc_sw128(sb + kk * 32, 16, 1024);
               const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
               if constexpr (kTF32) {
                 const uint64_t ad_lo = smem_desc_sw128(sa + C::kA + kk * 32, 16, 1024);
@@ -539,7 +504,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
                 mma<true, kCL>(d_tmem, ad, bd_lo, idesc, 1u);
                 mma<true, kCL>(d_tmem, ad, bd, idesc, 1u);
               } else {
-                mma<false, kCL>(d_tmem, ad, bd, id, accumulate);
+                mma<false, kCL>(d_tmem, ad, bd, idesc, accumulate);
               }
             }
             if constexpr (kCL > 1) mma_commit_multicast<kCL>(&empty_bar[stage], kPair);
@@ -715,16 +680,15 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
             for (int j = 0; j < 32; ++j)
               if (j == lane) v[j] += a.diag;
           }
-          // Every chunk of a tile leaves as one TMA box.  GRAM stores A as the
-          // 256-blocks its tiles cover (on and above the diagonal), which POLY
-          // reads transposed where needed; POLY also writes the transpose of a
-          // chunk above the diagonal blocks (row block left of the column block),
-          // so that B' is whole and UPDATE reads its rows in place.
+          // Every chunk of a tile leaves as one TMA box.  The symmetric products
+          // also write the transpose of a chunk above the diagonal blocks (row
+          // block left of the column block); the diagonal blocks are computed and
+          // written whole, so A and B' are whole for the next GEMM.
           if (row0 >= G.M) {
             __syncwarp();
             continue;
           }
-          const bool mirror = mode == kPoly && (row0 >> 8) < (c0 >> 8);
+          const bool mirror = mode != kUpdate && (row0 >> 8) < (c0 >> 8);
           if (lane == 0) bulk_wait_group_read<0>();  // the last boxes have left the staging
           __syncwarp();
 #pragma unroll

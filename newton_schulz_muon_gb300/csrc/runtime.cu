@@ -91,7 +91,6 @@ struct BGroup {
   CUtensorMap kx_lo[2], mx_lo[2], ka_lo, kb_lo;
   CUtensorMap kxt[2], kxt_lo[2];
   CUtensorMap ex[2], ea, eb;  // bf16 GEMM epilogue boxes of 32 x 32 (64-byte swizzle)
-  CUtensorMap ma;             // bf16 A in MN-major boxes {64, 64} (POLY's k blocks read transposed)
 };
 
 struct Bucket {
@@ -646,7 +645,7 @@ muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream
         } else if (mode == kPoly) {
           G.map_a = g.ka; G.map_b = g.ka;
           if (tf32) { G.map_a_lo = g.ka_lo; G.map_b_lo = g.ka_lo; }
-          if (!tf32) { G.map_c = g.eb; G.map_d = g.ea; G.map_a_mn = g.ma; G.map_b_mn = g.ma; }
+          if (!tf32) { G.map_c = g.eb; G.map_d = g.ea; }
           G.c_hi = ns + g.off_b; G.c_lo = lo(g.off_b_lo);
           G.d_hi = ns + g.off_a; G.d_lo = lo(g.off_a_lo);
           G.c_ld = g.ld_m; G.c_mstride = g.m * g.ld_m;
@@ -859,7 +858,6 @@ muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes
           ok &= encode_map(&g.ex[i], ns + g.off_x[i], es, g.n, g.m, g.count, g.ld_n, 32, 32, sw);
         ok &= encode_map(&g.ea, ns + g.off_a, es, g.m, g.m, g.count, g.ld_m, 32, 32, sw);
         ok &= encode_map(&g.eb, ns + g.off_b, es, g.m, g.m, g.count, g.ld_m, 32, 32, sw);
-        ok &= encode_map(&g.ma, ns + g.off_a, es, g.m, g.m, g.count, g.ld_m, kbox, kbox);
       }
       if (tf32) {
         for (int i = 0; i < 2; ++i) {

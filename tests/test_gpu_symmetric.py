@@ -1,9 +1,9 @@
-"""Symmetric products stored partly, against the fp64 oracle.
+"""Symmetric products written from their upper tiles, against the fp64 oracle.
 
-In bf16, A = X X^T is stored as the 256 x 256 blocks on and above the diagonal.
-POLY reads the k blocks left of an operand's row block transposed from there, and
-writes B' = aI + bA + cAA whole: its tiles above the diagonal blocks also go out as
-their transposes. UPDATE reads B' rows in place.
+In bf16 the GRAM and POLY launches compute only the 256 x 256 blocks on and above
+the diagonal. A diagonal block is written whole, and a block above it also writes
+its transpose, so A and B' = aI + bA + cAA are whole when the next GEMM reads their
+rows in place.
 
 The shapes cover:
 - ragged 256-blocks (m not a multiple of 256), down to a last block of one row;
@@ -14,7 +14,7 @@ The shapes cover:
 Single iterations with chosen coefficients isolate each product:
 - (1, 0, 0): B' = I, so the UPDATE epilogue stands alone;
 - (0, 1, 0): B' = A, copied whole by POLY's epilogue;
-- (0, 0, 1): POLY's transposed reads of both operands.
+- (0, 0, 1): A A, both operands read from the mirrored A.
 """
 import pytest
 
