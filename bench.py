@@ -341,6 +341,32 @@ def ns_kernel_name(nsm, plan, info):
     return "ns_gemm_kernel and ns_small_kernel (bf16, with the fused weight update)"
 
 
+def roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, ns_bytes, ns_alg_tflops,
+                   peak_tf, peak_name, peaks, bf16_sustained, traffic):
+    """The roofline object of the Newton-Schulz phase's dominant kernel, per launch."""
+    mult = 3 if tf32 else 1
+    tensor_frac = ns_alg_tflops * mult / peak_tf
+    out = {"kernel": ns_kernel_name(nsm, plan, info) + (", 3xTF32" if tf32 else ""),
+           "per_launch_ms": ns_ms / ns_launches}
+    if hbm_bound:
+        gbs = ns_bytes / (ns_ms * 1e-3) / 1e9
+        out.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "traffic": traffic,
+                    "peak_kind": "measured HBM copy bandwidth",
+                    "algorithmic_bytes_per_launch": ns_bytes / ns_launches,
+                    "bytes_counted": "X0 read (bf16) + weights read + weights written",
+                    "tensor_frac": tensor_frac, "tensor_peak_kind": peak_name})
+    else:
+        out.update({"bound": "tensor", "achieved": ns_alg_tflops * mult, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": tensor_frac, "traffic": traffic, "peak_kind": peak_name,
+                    "algorithmic_flops_per_launch": algorithmic / ns_launches})
+        if not tf32:
+            out["frac_of_burst"] = ns_alg_tflops / peaks["bf16_tflops"]
+            out["frac_of_sustained"] = ns_alg_tflops / bf16_sustained
+    out["traffic_unit"] = "bytes per launch (dram read + write, one ncu capture)"
+    return out
+
+
 def workload_spec(name, layers=None):
     """Tensors (rows, cols, count), dtypes, distributions and bucket cap of a workload.
     `layers` shortens the per-head and expert workloads (for profiling captures)."""
@@ -457,13 +483,32 @@ def run_gpu(args):
                      for i in range(len(tensors)))
     prep_bytes = sum(G[i].numel() * (G[i].element_size() + 4 + 4 + 2) for i in range(len(tensors)))
     peaks, peak_kind = load_peaks()
-    peak_tf = bf16_sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    bf16_sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # The burst figure for a kernel that ran at full clock in a short timed region,
+    # the sustained one where the power cap held the clock down or the timed region
+    # lasted seconds (the sustained figure was taken over a 4 s loop).
+    timed_s = ms * 1e-3 * args.steps
+    sustained = "sw_power_cap" in clocks.get("reasons", []) or timed_s >= 2.0
+    peak_tf = bf16_sustained if sustained else peaks["bf16_tflops"]
+    peak_name = (f"{peak_kind} bf16 sustained (power cap active or a timed region of seconds: {timed_s:.2f} s)"
+                 if sustained else
+                 f"{peak_kind} bf16 burst (no power cap seen, timed region {timed_s:.2f} s)")
     ns_alg_tflops = algorithmic / (ns_ms * 1e-3) / 1e12
     if tf32:
         # 3xTF32: three kind::tf32 products per product; the tf32 peak is the measured
         # bf16 figure times the nominal tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)
         peak_tf = peak_tf * 1.1 / 2.25
+        peak_name = f"{peak_name} x 1.1/2.25 (nominal tf32/bf16); achieved counts the three tf32 products of each product"
     ns_launches = launches_per_step(nsm, plan, info) - 2 * info.n_buckets
+    # the single-launch kernel for m <= 128 reads X0 once and the weights once and
+    # writes the weights once (A, B' and the iterations' X stay on chip or in the
+    # L2 at best): when those bytes take longer at the HBM peak than the products
+    # at the tensor peak, HBM is its roofline
+    single_kernel = all(nsm.muon_get_bucket_info(plan, b).ns_single_kernel for b in range(info.n_buckets))
+    ns_bytes = sum(k * min(r, c) * max(r, c) * 2 + 2 * W[i].numel() * W[i].element_size()
+                   for i, (r, c, k) in enumerate(tensors))
+    hbm_bound = (single_kernel and not tf32 and
+                 ns_bytes / (peaks["hbm_gbs"] * 1e9) > algorithmic / (peak_tf * 1e12))
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step uploads that step's gradients from pinned host memory (on a copy
@@ -548,16 +593,9 @@ def run_gpu(args):
                      "note": "the weight update runs in the last UPDATE GEMM's epilogue"},
         "elementwise_gbs": {"prep": prep_bytes / (prep_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                             "prep_frac": prep_bytes / (prep_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-        "roofline": {"bound": "tensor", "kernel": ns_kernel_name(nsm, plan, info) + (", 3xTF32" if tf32 else ""),
-                     "achieved": ns_alg_tflops * (3 if tf32 else 1), "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": ns_alg_tflops * (3 if tf32 else 1) / peak_tf,
-                     "traffic": ns_gemm_traffic() if args.workload == "layer" and not tf32 else None,
-                     "traffic_unit": "bytes per launch (dram read + write, one ncu capture)",
-                     "peak_kind": (f"{peak_kind} bf16 sustained x 1.1/2.25 (nominal tf32/bf16); achieved counts "
-                                   "the three tf32 products of each product" if tf32 else
-                                   f"{peak_kind} bf16 sustained (kernel runs inside multi-second loops)"),
-                     "per_launch_ms": ns_ms / ns_launches,
-                     "algorithmic_flops_per_launch": algorithmic / ns_launches},
+        "roofline": roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, ns_bytes,
+                                   ns_alg_tflops, peak_tf, peak_name, peaks, bf16_sustained,
+                                   ns_gemm_traffic() if args.workload == "layer" and not tf32 else None),
         "clocks": clocks,
         "gpu_launches": args.steps * launches_per_step(nsm, plan, info),
     }
