@@ -225,6 +225,15 @@ size_t muon_noalloc_scratch_bytes(void);
  * else MUON_OK.  n_nonfinite may be NULL. */
 muon_status muon_sync(muon_plan_t* plan, void* stream, int64_t* n_nonfinite);
 
+/* Self-test of the device failure path.  Enqueues on `stream` one CTA that waits
+ * on an mbarrier nothing arrives on, through the same bounded wait the
+ * Newton-Schulz kernels use, and gives up after limit_us microseconds (1 ..
+ * 1000000).  The timeout is recorded in the plan's device status word, so the
+ * next muon_sync returns MUON_ERR_DEVICE (and clears it); nothing faults and the
+ * context stays usable.  Errors: MUON_ERR_INVALID (NULL plan, limit out of range),
+ * MUON_ERR_NO_WORKSPACE, MUON_ERR_CUDA. */
+muon_status muon_selftest_wait_timeout(muon_plan_t* plan, int64_t limit_us, void* stream);
+
 /* Plan layout, for logging and tests (pure host). */
 typedef struct {
   int64_t n_tensors;

@@ -84,6 +84,7 @@ def _load() -> ctypes.CDLL:
         "muon_offload_step": (c_int32, [P, POINTER(P), POINTER(P), POINTER(P), c_int64, c_float,
                                         c_int32, c_int32, P, P, c_int64]),
         "muon_sync": (c_int32, [P, P, POINTER(c_int64)]),
+        "muon_selftest_wait_timeout": (c_int32, [P, c_int64, P]),
         "muon_get_plan_info": (c_int32, [P, POINTER(muon_plan_info)]),
         "muon_get_bucket_info": (c_int32, [P, c_int64, POINTER(muon_bucket_info)]),
         "muon_set_ns_schedule": (c_int32, [P, POINTER(c_float), c_int32]),
@@ -242,6 +243,13 @@ def muon_sync(plan: Plan, stream=None):
     nf = c_int64()
     st = _check(_lib().muon_sync(plan.handle, _stream_ptr(stream), byref(nf)), "muon_sync")
     return st, nf.value
+
+
+def muon_selftest_wait_timeout(plan: Plan, limit_us: int, stream=None) -> None:
+    """Enqueue the failure-path self-test: a one-CTA kernel whose bounded wait runs
+    out after limit_us; the next muon_sync reports it (MUON_ERR_DEVICE)."""
+    _check(_lib().muon_selftest_wait_timeout(plan.handle, int(limit_us), _stream_ptr(stream)),
+           "muon_selftest_wait_timeout")
 
 
 def muon_get_plan_info(plan: Plan) -> muon_plan_info:

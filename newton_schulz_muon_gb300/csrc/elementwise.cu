@@ -386,7 +386,27 @@ __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__
   }
 }
 
+// The failure-path self-test: one thread waits on an mbarrier whose phase nothing
+// completes, with the bounded wait every kernel of the library uses, which gives up
+// after limit_ns and sets kStatusWaitTimeout in the device status word.
+__global__ void wait_selftest_kernel(DeviceStatus* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0u, &abort_flag, &status->flags, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(DeviceStatus* status, unsigned long long limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
   if (a.total_tiles <= 0) return cudaSuccess;

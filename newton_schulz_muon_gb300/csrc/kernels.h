@@ -172,6 +172,9 @@ constexpr int kBN = 256;
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_norm(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t s);
+// One CTA waiting on a barrier nothing arrives on, for limit_ns, through the
+// kernels' bounded wait: records the timeout in *status (the failure-path self-test).
+cudaError_t launch_wait_selftest(DeviceStatus* status, unsigned long long limit_ns, cudaStream_t s);
 // cluster: 1, or 2 (pairs of vertically adjacent tiles share the B operand);
 // GemmGroup::tiles_m counts row blocks of kBM * cluster rows.
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, int cluster, cudaStream_t s);

@@ -1210,6 +1210,16 @@ muon_status muon_sync(muon_plan_t* p, void* stream, int64_t* n_nonfinite) {
   return MUON_OK;
 }
 
+muon_status muon_selftest_wait_timeout(muon_plan_t* p, int64_t limit_us, void* stream) {
+  if (!p) return fail(MUON_ERR_INVALID, "plan is NULL");
+  if (limit_us < 1 || limit_us > 1000000) return fail(MUON_ERR_INVALID, "limit_us must be in [1, 1000000]");
+  if (!p->ws) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
+  cudaError_t e = launch_wait_selftest(at<DeviceStatus>(p, p->off_status), (unsigned long long)limit_us * 1000ull,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return MUON_OK;
+}
+
 muon_status muon_get_stats(const muon_plan_t* p, muon_stats* out) {
   if (!p || !out) return fail(MUON_ERR_INVALID, "NULL argument");
   std::memset(out, 0, sizeof(*out));

@@ -151,6 +151,15 @@ def test_step_without_workspace_is_refused(nsm):
     assert st == nsm.MUON_ERR_NO_WORKSPACE
 
 
+def test_selftest_arguments_are_checked(nsm):
+    p = nsm.muon_plan([(8, 16)])
+    assert nsm.lib.muon_selftest_wait_timeout(None, 1000, None) == nsm.MUON_ERR_INVALID
+    for bad in (0, -5, 1_000_001):
+        assert nsm.lib.muon_selftest_wait_timeout(p.handle, bad, None) == nsm.MUON_ERR_INVALID
+    # no workspace bound: refused before anything is enqueued
+    assert nsm.lib.muon_selftest_wait_timeout(p.handle, 1000, None) == nsm.MUON_ERR_NO_WORKSPACE
+
+
 def test_status_strings(nsm):
     for code in (0, 1, -1, -2, -3, -4, -5, -6, -7):
         assert nsm.muon_status_string(code)

@@ -150,6 +150,30 @@ def test_argument_validation_on_device(m):
     assert e.value.status == m.MUON_ERR_NO_WORKSPACE
 
 
+def test_device_wait_timeout_is_reported_and_the_context_stays_usable(m):
+    # the failure path without a fault: a kernel's bounded wait runs out (a
+    # barrier nothing arrives on, 20 ms limit), the status word records it,
+    # muon_sync reports and clears it, and the next steps run and match the oracle
+    import time
+    import torch
+    wl = Workload([(128, 640), (300, 200)], m_sigma=0.02, g_sigma=1e-3)
+    plan = m.muon_plan(wl.plan_shapes())
+    m.allocate_workspace(plan)
+    t0 = time.perf_counter()
+    m.muon_selftest_wait_timeout(plan, 20_000)
+    with pytest.raises(m.MuonError) as e:
+        m.muon_sync(plan)
+    waited = time.perf_counter() - t0
+    assert e.value.status == m.MUON_ERR_DEVICE
+    assert 0.015 <= waited < 5.0
+    assert m.muon_sync(plan) == (m.MUON_OK, 0)  # cleared by the read
+    m.muon_step(plan, wl.dW, wl.dG, wl.dM, 0.02, 0.95, True, 0.0, 5)  # the same plan steps on
+    assert m.muon_sync(plan) == (m.MUON_OK, 0)
+    torch.cuda.synchronize()
+    ulp, rel = run_steps(m, wl, steps=2)
+    assert ulp <= 1 and rel <= TOL_BF16
+
+
 # --- fp32 (3xTF32) Newton-Schulz mode: per-matrix tolerance 1e-4 --------------
 
 @pytest.mark.parametrize("shapes", [[(256, 512)], [(300, 200), (100, 700)], [(128, 384, 3), (640, 384)],
