@@ -296,7 +296,7 @@ class ClockSampler:
 # over the 15 launches of one step, from one ncu capture (the command and the
 # per-launch table are in profiles/ns_gemm_qwen3_4b_layer.md).  Valid only for the
 # kernel sources it was taken on: the bench reports null once their digest moves.
-NS_GEMM_TRAFFIC = {"bytes_per_launch": 350.9e6, "sources_sha256_16": "0485ca8c280985e4"}
+NS_GEMM_TRAFFIC = {"bytes_per_launch": 348.4e6, "sources_sha256_16": "cd159d403de38d75"}
 KERNEL_SOURCES = ("newton_schulz_muon_gb300/csrc/ns_gemm.cu", "newton_schulz_muon_gb300/csrc/device.cuh",
                   "newton_schulz_muon_gb300/csrc/kernels.h", "newton_schulz_muon_gb300/csrc/epilogue.cuh")
 
