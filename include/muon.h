@@ -52,7 +52,7 @@ typedef int32_t muon_status;
 #define MUON_ERR_NO_WORKSPACE (-3) /* no workspace bound, or it is too small */
 #define MUON_ERR_CUDA (-4)      /* a CUDA runtime/driver call failed */
 #define MUON_ERR_TIMEOUT (-5)   /* a bounded host wait ran out */
-#define MUON_ERR_UNSUPPORTED (-6) /* option not available in this build / device */
+#define MUON_ERR_UNSUPPORTED (-6) /* option not supported by the library or the device */
 #define MUON_ERR_DEVICE (-7)    /* a kernel's bounded wait ran out (device status word) */
 
 /* element types */
