@@ -559,6 +559,9 @@ void ns_coeffs(const muon_plan_t* p, int k, float out[3]) {
   for (int j = 0; j < 3; ++j) out[j] = p->ns_sched[3 * i + j];
 }
 
+static_assert(sizeof(SmallArgs::coef) / sizeof(SmallArgs::coef[0]) == MUON_MAX_NS_STEPS,
+              "one coefficient triple per possible iteration");
+
 muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st,
                              const ApplyArgs& fused) {
   SmallArgs sa;
@@ -791,7 +794,7 @@ muon_status muon_get_plan_info(const muon_plan_t* plan, muon_plan_info* info) {
 
 muon_status muon_set_ns_schedule(muon_plan_t* plan, const float* coeffs, int32_t n_iters) {
   if (!plan) return fail(MUON_ERR_INVALID, "NULL plan");
-  if (n_iters < 0 || n_iters > MUON_MAX_NS_STEPS) return fail(MUON_ERR_INVALID, "n_iters must be in [0, 16]");
+  if (n_iters < 0 || n_iters > MUON_MAX_NS_STEPS) return fail(MUON_ERR_INVALID, "n_iters must be in [0, %d]", MUON_MAX_NS_STEPS);
   if (n_iters > 0 && !coeffs) return fail(MUON_ERR_INVALID, "NULL coefficients");
   for (int i = 0; i < 3 * n_iters; ++i)
     if (!std::isfinite(coeffs[i])) return fail(MUON_ERR_INVALID, "coefficient %d is not finite", i);
@@ -924,7 +927,7 @@ muon_status muon_step(muon_plan_t* p, void* const* params, const void* const* gr
   if (!params || !grads || !momentum) return fail(MUON_ERR_INVALID, "pointer array is NULL");
   if (n_mats != (int64_t)p->tensors.size())
     return fail(MUON_ERR_INVALID, "n_mats %lld != %zu tensors in the plan", (long long)n_mats, p->tensors.size());
-  if (ns_steps < 0 || ns_steps > 16) return fail(MUON_ERR_INVALID, "ns_steps must be in [0, 16]");
+  if (ns_steps < 0 || ns_steps > MUON_MAX_NS_STEPS) return fail(MUON_ERR_INVALID, "ns_steps must be in [0, %d]", MUON_MAX_NS_STEPS);
   if (!std::isfinite(lr) || !std::isfinite(mu) || !std::isfinite(wd)) return fail(MUON_ERR_INVALID, "lr, mu, wd must be finite");
   for (int i = 0; i < n_mats; ++i) {
     muon_status s;
@@ -1078,7 +1081,7 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
   if (!h_grads || !h_momentum || !h_update_out) return fail(MUON_ERR_INVALID, "pointer array is NULL");
   if (n_mats != (int64_t)p->tensors.size())
     return fail(MUON_ERR_INVALID, "n_mats %lld != %zu tensors in the plan", (long long)n_mats, p->tensors.size());
-  if (ns_steps < 0 || ns_steps > 16) return fail(MUON_ERR_INVALID, "ns_steps must be in [0, 16]");
+  if (ns_steps < 0 || ns_steps > MUON_MAX_NS_STEPS) return fail(MUON_ERR_INVALID, "ns_steps must be in [0, %d]", MUON_MAX_NS_STEPS);
   if (timeout_ms <= 0) return fail(MUON_ERR_INVALID, "timeout_ms must be > 0");
   for (int i = 0; i < n_mats; ++i) {
     muon_status s;
