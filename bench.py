@@ -341,6 +341,24 @@ def ns_kernel_name(nsm, plan, info):
     return "ns_gemm_kernel and ns_small_kernel (bf16, with the fused weight update)"
 
 
+def choose_bf16_peak(peaks, peak_kind, clocks, timed_s):
+    """The bf16 denominator: the burst figure for a kernel that ran at full clock in
+    a short timed region, the sustained one where the power cap held the clock down
+    or the timed region lasted seconds (the sustained figure was taken over a 4 s
+    loop).  Returns (TFLOP/s, description)."""
+    sustained = "sw_power_cap" in clocks.get("reasons", []) or timed_s >= 2.0
+    if sustained:
+        return (peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+                f"{peak_kind} bf16 sustained (power cap active or a timed region of seconds: {timed_s:.2f} s)")
+    return peaks["bf16_tflops"], f"{peak_kind} bf16 burst (no power cap seen, timed region {timed_s:.2f} s)"
+
+
+def hbm_binds(nbytes, flops, hbm_gbs, tensor_tflops):
+    """True when moving `nbytes` at the HBM peak takes longer than `flops` at the
+    tensor peak: the roofline of that kernel is HBM."""
+    return nbytes / (hbm_gbs * 1e9) > flops / (tensor_tflops * 1e12)
+
+
 def roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, ns_bytes, ns_alg_tflops,
                    peak_tf, peak_name, peaks, bf16_sustained, traffic):
     """The roofline object of the Newton-Schulz phase's dominant kernel, per launch."""
@@ -484,15 +502,7 @@ def run_gpu(args):
     prep_bytes = sum(G[i].numel() * (G[i].element_size() + 4 + 4 + 2) for i in range(len(tensors)))
     peaks, peak_kind = load_peaks()
     bf16_sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    # The burst figure for a kernel that ran at full clock in a short timed region,
-    # the sustained one where the power cap held the clock down or the timed region
-    # lasted seconds (the sustained figure was taken over a 4 s loop).
-    timed_s = ms * 1e-3 * args.steps
-    sustained = "sw_power_cap" in clocks.get("reasons", []) or timed_s >= 2.0
-    peak_tf = bf16_sustained if sustained else peaks["bf16_tflops"]
-    peak_name = (f"{peak_kind} bf16 sustained (power cap active or a timed region of seconds: {timed_s:.2f} s)"
-                 if sustained else
-                 f"{peak_kind} bf16 burst (no power cap seen, timed region {timed_s:.2f} s)")
+    peak_tf, peak_name = choose_bf16_peak(peaks, peak_kind, clocks, ms * 1e-3 * args.steps)
     ns_alg_tflops = algorithmic / (ns_ms * 1e-3) / 1e12
     if tf32:
         # 3xTF32: three kind::tf32 products per product; the tf32 peak is the measured
@@ -507,8 +517,7 @@ def run_gpu(args):
     single_kernel = all(nsm.muon_get_bucket_info(plan, b).ns_single_kernel for b in range(info.n_buckets))
     ns_bytes = sum(k * min(r, c) * max(r, c) * 2 + 2 * W[i].numel() * W[i].element_size()
                    for i, (r, c, k) in enumerate(tensors))
-    hbm_bound = (single_kernel and not tf32 and
-                 ns_bytes / (peaks["hbm_gbs"] * 1e9) > algorithmic / (peak_tf * 1e12))
+    hbm_bound = single_kernel and not tf32 and hbm_binds(ns_bytes, algorithmic, peaks["hbm_gbs"], peak_tf)
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step uploads that step's gradients from pinned host memory (on a copy
