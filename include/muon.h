@@ -116,7 +116,14 @@ typedef struct {
  * offload 0, ns_kernel MUON_NS_KERNEL_AUTO. */
 void muon_config_default(muon_config* cfg);
 
-/* Builds the host plan: orients each logical matrix (wide form m x n, m <= n,
+/* Defines: "Muon Optimizer + FSDP", section 分块通信 (chunked communication:
+ * same-shape matrices bucketed together, fused [Q;K;V] and [E,out,in] tensors
+ * split into logical matrices first) and section 推荐的分块执行伪代码 (recommended
+ * chunked-execution pseudocode: plan_micro_buckets(bucket, cap_bytes, cost_fn));
+ * section 内存控制方案 items 1 (a byte cap per micro-bucket) and 6 (same-shape
+ * expert buckets across layers); DeepSpeed issue "[RFC] ... ZeRO CPU Offload",
+ * section 4.A (shapes and head dimensions carried into the optimizer).
+ * Builds the host plan: orients each logical matrix (wide form m x n, m <= n,
  * transposed when rows > cols), groups matrices by (group label, m, n), and
  * packs whole matrices, in order, into micro-buckets whose wide-form bf16 bytes
  * (m*n*2 summed) stay <= bucket_cap_bytes.  A matrix larger than the cap gets a
@@ -130,11 +137,15 @@ void muon_config_default(muon_config* cfg);
 muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t* groups,
                       int64_t bucket_cap_bytes, const muon_config* cfg, muon_plan_t** out);
 
-/* Device workspace the plan needs (bytes, 256-byte aligned use), including the
+/* Defines: "Muon Optimizer + FSDP", section 内存控制方案 item 2 (one persistent
+ * preallocated workspace reused by every bucket; MuonWorkspace in section
+ * 推荐的分块执行伪代码).
+ * Device workspace the plan needs (bytes, 256-byte aligned use), including the
  * offload staging slots.  Pure host work. */
 muon_status muon_plan_workspace_bytes(const muon_plan_t* plan, size_t* device_bytes);
 
-/* Binds caller-allocated device memory of at least muon_plan_workspace_bytes,
+/* Defines: as muon_plan_workspace_bytes (the caller allocates, the plan reuses).
+ * Binds caller-allocated device memory of at least muon_plan_workspace_bytes,
  * 256-byte aligned, on the current device.  Encodes the TMA tensor maps over
  * it and creates the plan's events/streams.  The memory must outlive every
  * enqueued step.  Errors: MUON_ERR_INVALID, MUON_ERR_NO_WORKSPACE, MUON_ERR_CUDA,
@@ -165,7 +176,11 @@ muon_status muon_set_ns_schedule(muon_plan_t* plan, const float* coeffs, int32_t
 muon_status muon_polar_express_coefficients(int32_t n_iters, double lower, double safety, float* coeffs_out,
                                             double* err_out);
 
-/* One Muon step over every matrix of the plan, enqueued on `stream`.
+/* Defines: "Muon Optimizer + FSDP", section 背景 (background: M_t =
+ * momentum_update(grad), U_t = NewtonSchulz(M_t), W_t = W_t - lr U_t on each full
+ * 2-D matrix); DeepSpeed issue "[RFC] ... ZeRO CPU Offload", section 2 (5-6
+ * Newton-Schulz iterations on full 2-D weight matrices).
+ * One Muon step over every matrix of the plan, enqueued on `stream`.
  *   params[n_mats]:   device pointers, weights (cfg.param_dtype), updated in place.
  *   grads[n_mats]:    device pointers, gradients (cfg.grad_dtype), read only.
  *   momentum[n_mats]: device pointers, fp32 momentum, updated in place.
@@ -180,7 +195,12 @@ muon_status muon_step(muon_plan_t* plan, void* const* params, const void* const*
                       void* const* momentum, int64_t n_mats, float lr, float mu,
                       int32_t nesterov, float wd, int32_t ns_steps, void* stream);
 
-/* Offload step: gradients and fp32 momentum live in page-locked host memory.
+/* Defines: DeepSpeed PR "[Muon] CPU offload: pin the momentum and overlap the
+ * host writeback", sections Motivation (gradient and momentum copied to the
+ * device, update and momentum back, every step) and Changes (pinned momentum; the
+ * writeback of batch i on a side stream after batch i+1 is queued; at most one
+ * batch computed and one in flight; drained before the host reads).
+ * Offload step: gradients and fp32 momentum live in page-locked host memory.
  * Per micro-bucket: host->device copy of G and M on a private copy stream,
  * momentum + Newton-Schulz on `compute`, then device->host writeback of the new
  * momentum (into h_momentum) and of the update U' = sqrt(max(1,rows/cols)) * U
@@ -197,10 +217,11 @@ muon_status muon_offload_step(muon_plan_t* plan, const void* const* h_grads,
                               int64_t n_mats, float mu, int32_t nesterov, int32_t ns_steps,
                               void* compute, void* copy, int64_t timeout_ms);
 
-/* muon_step for callers that cannot allocate device memory (code running inside
- * an allocator or memory-pool callback, a runtime that has given all device
- * memory to its own pool, a plugin host that forbids device allocations).  The
- * sources describe no such variant; it has no counterpart there.
+/* muon_step for callers that cannot allocate device memory: code running inside
+ * an allocator or memory-pool callback (which must not re-enter the allocator),
+ * a runtime that has given all device memory to its own pool, a plugin host that
+ * forbids device allocations.  The sources describe no such variant; it has no
+ * counterpart there.
  * Same arguments and results as muon_step, but no workspace is bound by the
  * caller: the step runs in a file-scope device array of the library
  * (muon_noalloc_scratch_bytes(), 64 MiB), which every GPU that loads the library
@@ -208,10 +229,19 @@ muon_status muon_offload_step(muon_plan_t* plan, const void* const* h_grads,
  * no allocating library routine).
  *   - The first call on a device, with that device current, looks up the array's
  *     address (cudaGetSymbolAddress); make it before any stream capture.
- *   - Each call binds `plan` to the array (tensor maps, status word cleared).
+ *   - The array remembers the plan it was last bound to.  A call with another
+ *     plan re-binds it: tensor maps encoded on the host, and the plan's tile
+ *     schedules copied into the array on `stream`, after the work already
+ *     enqueued there (the copy may block the host while the driver stages it).
+ *     Calls with the same plan bind nothing.
+ *   - The device status word in the array starts at zero and is shared by every
+ *     plan that runs in it: calls never clear it, so it keeps counting
+ *     (non-finite matrices, bounded waits that ran out) until muon_sync on any
+ *     of those plans reads and clears it.
  *   - Plans whose workspace exceeds the array: MUON_ERR_NO_WORKSPACE.
  *   - All calls share the array and it keeps the last call's contents: calls
- *     whose device work overlaps race on it; serialise them. */
+ *     whose device work overlaps race on it.  Enqueue them on one stream, or make
+ *     each call's stream wait for the previous call's work. */
 muon_status muon_step_noalloc(muon_plan_t* plan, void* const* params, const void* const* grads,
                               void* const* momentum, int64_t n_mats, float lr, float mu,
                               int32_t nesterov, float wd, int32_t ns_steps, void* stream);
@@ -219,7 +249,10 @@ muon_status muon_step_noalloc(muon_plan_t* plan, void* const* params, const void
 /* Size in bytes of the static array muon_step_noalloc works in. */
 size_t muon_noalloc_scratch_bytes(void);
 
-/* Waits for `stream`, then reads and clears the device status word written by
+/* Defines: DeepSpeed issue "[RFC] ... ZeRO CPU Offload", section 5 (overflow
+ * skipping named among the interactions of the step); the status word itself is
+ * this library's.
+ * Waits for `stream`, then reads and clears the device status word written by
  * the kernels: MUON_ERR_DEVICE if a kernel's bounded wait ran out,
  * MUON_WARN_NONFINITE (with *n_nonfinite set) if a matrix norm was not finite,
  * else MUON_OK.  n_nonfinite may be NULL. */
@@ -234,7 +267,9 @@ muon_status muon_sync(muon_plan_t* plan, void* stream, int64_t* n_nonfinite);
  * MUON_ERR_NO_WORKSPACE, MUON_ERR_CUDA. */
 muon_status muon_selftest_wait_timeout(muon_plan_t* plan, int64_t limit_us, void* stream);
 
-/* Plan layout, for logging and tests (pure host). */
+/* Defines: "Muon Optimizer + FSDP", section 需要记录的指标 (metrics to log per
+ * Muon bucket: key, logical shape, tensor counts, bytes, workspace bytes).
+ * Plan layout, for logging and tests (pure host). */
 typedef struct {
   int64_t n_tensors;
   int64_t n_matrices;
@@ -246,7 +281,8 @@ typedef struct {
 } muon_plan_info;
 muon_status muon_get_plan_info(const muon_plan_t* plan, muon_plan_info* info);
 
-/* Bucket b: number of matrices, wide-form bf16 bytes, same-shape groups in it,
+/* Defines: as muon_get_plan_info, per bucket.
+ * Bucket b: number of matrices, wide-form bf16 bytes, same-shape groups in it,
  * the (m, n) of its first group, and whether its Newton-Schulz iterations run
  * in the single small-matrix kernel (1: every group has m <= 128, bf16
  * arithmetic, ns_kernel AUTO) or as grouped GEMM launches (0). */
@@ -259,7 +295,9 @@ typedef struct {
 } muon_bucket_info;
 muon_status muon_get_bucket_info(const muon_plan_t* plan, int64_t b, muon_bucket_info* info);
 
-/* Timings of the last step (cfg.timing = 1), summed over buckets, in ms:
+/* Defines: "Muon Optimizer + FSDP", section 需要记录的指标 (per-bucket times:
+ * newton_schulz_time_ms and the transfer times around it).
+ * Timings of the last step (cfg.timing = 1), summed over buckets, in ms:
  * prep (momentum kernel), ns (all Newton-Schulz GEMMs), apply, h2d, d2h and the
  * whole step; plus bytes moved over the host link.  Synchronizes the events. */
 typedef struct {

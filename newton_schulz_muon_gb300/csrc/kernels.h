@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+struct muon_plan_s;
+
 namespace muon {
 
 constexpr int kMaxSegs = 64;     // runs of consecutive matrices of one tensor per bucket
@@ -188,5 +190,14 @@ constexpr int kSmallMaxRows = 128;
 
 // Records `msg` as the calling thread's muon_last_error text and returns `s`.
 int32_t set_error(int32_t s, const char* msg);
+
+// The no-allocation path (noalloc.cu).  bind_shared_scratch binds a plan to the
+// library's static scratch like muon_plan_bind_workspace, but copies the tile
+// schedules on `stream` (ordered after the work already enqueued there) and
+// leaves the device status word as it is; plan_id is a process-unique plan
+// number; plan_workspace the device memory the plan is bound to (or null).
+int32_t bind_shared_scratch(muon_plan_s* p, void* dev_ptr, size_t bytes, cudaStream_t stream);
+uint64_t plan_id(const muon_plan_s* p);
+const void* plan_workspace(const muon_plan_s* p);
 
 }  // namespace muon

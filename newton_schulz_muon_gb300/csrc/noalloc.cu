@@ -11,11 +11,22 @@
 //
 // Set-up: the first call on a device (with that device current) looks up the
 // array's device address with cudaGetSymbolAddress and caches it; make that
-// first call before any stream capture.  Each call then binds the plan to the
-// array (encoding its tensor maps and clearing the device status word, which
-// must start at zero) and enqueues muon_step.  All calls share the one array and
-// it keeps the last call's contents: calls whose work overlaps on the GPU race
-// on it, so serialise them (one stream, or wait between calls).
+// first call before any stream capture.
+//
+// Binding: the array remembers, per device, which plan it was last bound to.  A
+// call with that same plan binds nothing and goes straight to muon_step.  A call
+// with another plan re-binds: its tensor maps are encoded on the host and its
+// tile schedules are copied into the array on the caller's `stream`, so the copy
+// lands after the work already enqueued there (it may block the host while the
+// driver stages it from pageable memory).  The device status word at the start of
+// the array is zero when the library loads and is never cleared here: it is
+// shared by every plan that runs in the array and keeps counting (non-finite
+// matrices, bounded waits that ran out) until muon_sync on any of those plans
+// reads and clears it.
+//
+// All calls share the one array and it keeps the last call's contents, so calls
+// whose device work overlaps race on it: enqueue them on one stream, or make each
+// call's stream wait for the previous call's work.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -30,7 +41,11 @@ constexpr size_t kScratchBytes = 64ull << 20;  // 64 MiB
 __device__ __align__(256) unsigned char g_muon_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct DeviceScratch {
+  void* ptr = nullptr;    // device address of g_muon_scratch on this device
+  uint64_t owner = 0;     // id of the plan last bound to it (0: none)
+};
+DeviceScratch g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
 }  // namespace
@@ -53,20 +68,24 @@ muon_status muon_step_noalloc(muon_plan_t* plan, void* const* params, const void
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return muon::set_error(MUON_ERR_CUDA, cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return muon::set_error(MUON_ERR_UNSUPPORTED, "device ordinal out of range");
-  void* ptr = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    DeviceScratch& d = g_scratch[dev];
+    if (d.ptr == nullptr) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_muon_scratch);
       if (e != cudaSuccess || p == nullptr)
         return muon::set_error(MUON_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
-      g_scratch_ptr[dev] = p;
+      d.ptr = p;
     }
-    ptr = g_scratch_ptr[dev];
+    const bool bound = d.owner == muon::plan_id(plan) && muon::plan_workspace(plan) == d.ptr;
+    if (!bound) {
+      d.owner = 0;
+      s = muon::bind_shared_scratch(plan, d.ptr, kScratchBytes, static_cast<cudaStream_t>(stream));
+      if (s != MUON_OK) return s;
+      d.owner = muon::plan_id(plan);
+    }
   }
-  s = muon_plan_bind_workspace(plan, ptr, kScratchBytes);
-  if (s != MUON_OK) return s;
   return muon_step(plan, params, grads, momentum, n_mats, lr, mu, nesterov, wd, ns_steps, stream);
 }
 

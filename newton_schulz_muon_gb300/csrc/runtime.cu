@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstdarg>
@@ -146,6 +147,10 @@ struct muon_plan_s {
   int64_t last_h2d_bytes = 0, last_d2h_bytes = 0;
   // per-iteration (a, b, c) set by muon_set_ns_schedule; empty: cfg's for every iteration
   std::vector<float> ns_sched;
+  // process-unique id (never reused, unlike the plan's address)
+  uint64_t id = 0;
+  // the tile schedules as uploaded by the last bind (host copy kept for stream-ordered re-uploads)
+  std::vector<int32_t> sched_host;
 };
 
 namespace {
@@ -760,6 +765,8 @@ muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t*
     return fail(MUON_ERR_INVALID, "ns_kernel must be AUTO or GEMM");
   muon_plan_t* p = new (std::nothrow) muon_plan_t();
   if (!p) return fail(MUON_ERR_INVALID, "out of host memory");
+  static std::atomic<uint64_t> next_id{1};
+  p->id = next_id.fetch_add(1);
   p->cfg = c;
   p->cap = bucket_cap_bytes;
   muon_status s = build_plan(p, shapes, n_shapes, groups);
@@ -815,7 +822,16 @@ muon_status muon_get_bucket_info(const muon_plan_t* plan, int64_t b, muon_bucket
   return MUON_OK;
 }
 
-muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes) {
+}  // extern "C"
+
+namespace {
+
+// Binds `p` to `dev_ptr`: tensor maps, tile schedules, streams and events.
+// stream == nullptr (muon_plan_bind_workspace): the schedules are uploaded and the
+// status word cleared synchronously.  Otherwise (the shared static scratch): the
+// schedules are copied on `stream`, after the work already enqueued there, and
+// the status word is left alone.
+muon_status bind_impl(muon_plan_t* p, void* dev_ptr, size_t bytes, cudaStream_t stream, bool stream_ordered) {
   if (!p || !dev_ptr) return fail(MUON_ERR_INVALID, "NULL argument");
   if (reinterpret_cast<uintptr_t>(dev_ptr) & 255u) return fail(MUON_ERR_INVALID, "workspace must be 256-byte aligned");
   if (bytes < p->ws_bytes)
@@ -891,7 +907,11 @@ muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes
         std::copy(one.begin(), one.end(), host.begin() + b.sched_off[mode] / sizeof(int32_t));
         b.sched_clusters[mode] = clusters;
       }
-    e = cudaMemcpy(p->ws + p->off_sched, host.data(), p->sched_bytes, cudaMemcpyHostToDevice);
+    p->sched_host.swap(host);
+    e = stream_ordered ? cudaMemcpyAsync(p->ws + p->off_sched, p->sched_host.data(), p->sched_bytes,
+                                         cudaMemcpyHostToDevice, stream)
+                       : cudaMemcpy(p->ws + p->off_sched, p->sched_host.data(), p->sched_bytes,
+                                    cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "schedule upload");
   }
   if (!p->h2d_stream) {
@@ -915,9 +935,28 @@ muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes
     cudaEventCreate(&p->step_start);
     cudaEventCreate(&p->step_end);
   }
-  e = cudaMemset(p->ws + p->off_status, 0, sizeof(DeviceStatus));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  if (!stream_ordered) {
+    e = cudaMemset(p->ws + p->off_status, 0, sizeof(DeviceStatus));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();  // done before any stream's next kernel
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  }
   return MUON_OK;
+}
+
+}  // namespace
+
+int32_t muon::bind_shared_scratch(muon_plan_t* p, void* dev_ptr, size_t bytes, cudaStream_t stream) {
+  return bind_impl(p, dev_ptr, bytes, stream, true);
+}
+
+uint64_t muon::plan_id(const muon_plan_t* p) { return p ? p->id : 0; }
+
+const void* muon::plan_workspace(const muon_plan_t* p) { return p ? p->ws : nullptr; }
+
+extern "C" {
+
+muon_status muon_plan_bind_workspace(muon_plan_t* p, void* dev_ptr, size_t bytes) {
+  return bind_impl(p, dev_ptr, bytes, nullptr, false);
 }
 
 muon_status muon_step(muon_plan_t* p, void* const* params, const void* const* grads, void* const* momentum,
@@ -1202,11 +1241,16 @@ muon_status muon_sync(muon_plan_t* p, void* stream, int64_t* n_nonfinite) {
   if (!p->ws) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  // read and clear on `stream`, and wait for both: a memset on the legacy stream
+  // may still be pending when later work starts on a non-blocking stream
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   DeviceStatus ds;
-  e = cudaMemcpy(&ds, p->ws + p->off_status, sizeof(ds), cudaMemcpyDeviceToHost);
+  e = cudaMemcpyAsync(&ds, p->ws + p->off_status, sizeof(ds), cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
-  e = cudaMemset(p->ws + p->off_status, 0, sizeof(ds));
+  e = cudaMemsetAsync(p->ws + p->off_status, 0, sizeof(ds), st);
   if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   if (n_nonfinite) *n_nonfinite = ds.nonfinite;
   if (ds.flags) return fail(MUON_ERR_DEVICE, "a kernel gave up a bounded wait (status 0x%x)", ds.flags);
   if (ds.nonfinite) return MUON_WARN_NONFINITE;

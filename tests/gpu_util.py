@@ -10,6 +10,10 @@ import synth
 # per-matrix tolerances (relative Frobenius error of the update)
 TOL_BF16 = 3e-2
 TOL_TF32X3 = 1e-4
+# bf16 weights: the most the bf16-weight bound may allow, over ||dW||, in the tests
+# built to discriminate (W0 = 0, or an lr at which the update dominates the bf16
+# rounding of W): the 3e-2 tolerance plus at most 0.5e-2 of rounding allowance
+TOL_BF16_W = 3.5e-2
 
 
 def nsm():
@@ -112,11 +116,15 @@ class Workload:
 
 
 def check_step(wl: Workload, W_prev, M_prev, W_new, M_new, *, lr, mu, nesterov, wd, ns_steps,
-               coeffs=oracle.DEFAULT_COEFFS, eps=1e-7, form="ema", tol=TOL_BF16, sample=None):
+               coeffs=oracle.DEFAULT_COEFFS, eps=1e-7, form="ema", tol=TOL_BF16, sample=None,
+               bf16_max_bound=None):
     """Teacher-forced comparison of one GPU step against the oracle, per logical matrix.
 
     W_prev/M_prev are the host copies of the state the GPU started from; W_new/M_new
     what it produced.  Returns the worst (ulp, rel) seen; asserts the tolerances.
+    bf16 weights: ``bf16_max_bound`` also asserts that the bound applied stays
+    within that fraction of ||dW|| (the test discriminates), and rel is then the
+    measured error over ||dW||.
     """
     mu32, omu = oracle_constants(mu, form)
     c32 = f32_coeffs(coeffs)
@@ -132,8 +140,9 @@ def check_step(wl: Workload, W_prev, M_prev, W_new, M_new, *, lr, mu, nesterov, 
             ulp = int(ulp_distance(M_new[i][j], Mo).max())
             assert ulp <= 1, f"tensor {i} matrix {j}: momentum differs by {ulp} ulp"
             if wl.w_dtype == synth.BF16:
-                bf16_weight_check(W_new[i][j], Wo, Wp, tol)
-                rel = 0.0
+                rel = bf16_weight_check(W_new[i][j], Wo, Wp, tol, bf16_max_bound)
+                if bf16_max_bound is None:
+                    rel = 0.0
             else:
                 rel = rel_fro(widen(W_new[i][j], wl.w_dtype) - Wp, Wo - Wp)
                 assert rel <= tol, f"tensor {i} matrix {j} ({r}x{c}): rel update error {rel:.3e} > {tol:.1e}"
@@ -142,20 +151,25 @@ def check_step(wl: Workload, W_prev, M_prev, W_new, M_new, *, lr, mu, nesterov, 
     return worst_ulp, worst_rel
 
 
-def bf16_weight_check(W_new_bits, Wo, Wp, tol):
+def bf16_weight_check(W_new_bits, Wo, Wp, tol, max_bound=None):
     """bf16 weights: W_new = bf16(W_or + d) with ||d|| <= tol ||dW_or||, so
     ||W_new - W_or|| <= tol ||dW_or|| + || |W_or| 2^-8 || (a bf16 half-ulp is at most
-    2^-8 of the value).  Returns the measured left side over ||dW_or||."""
+    2^-8 of the value).  Returns the measured left side over ||dW_or||.
+    ``max_bound``: also assert that the bound is at most that fraction of
+    ||dW_or||, i.e. that the rounding allowance does not swamp the tolerance."""
     err = np.linalg.norm(synth.as_f64(W_new_bits, synth.BF16) - Wo)
     den = max(np.linalg.norm(Wo - Wp), 1e-30)
     bound = tol * den + np.linalg.norm(np.abs(Wo) * 2.0 ** -8)
     assert err <= bound, f"bf16 weights: error {err:.3e} above the bound {bound:.3e}"
+    if max_bound is not None:
+        assert bound <= max_bound * den, \
+            f"bf16 weights: the bound {bound / den:.3e} of ||dW|| is looser than {max_bound:.1e}"
     return float(err / den)
 
 
 def run_steps(m, wl, *, lr=0.02, mu=0.95, nesterov=True, wd=0.0, ns_steps=5, cap=512 << 20, cfg=None,
               steps=1, form="ema", coeffs=oracle.DEFAULT_COEFFS, sample=None, tol=TOL_BF16,
-              schedule=None):
+              schedule=None, bf16_max_bound=None):
     """Run `steps` GPU Muon steps on a Workload, checking each against the oracle.
     ``schedule``: per-iteration (a, b, c) set on the plan (and used by the oracle)
     in place of ``coeffs``."""
@@ -183,7 +197,8 @@ def run_steps(m, wl, *, lr=0.02, mu=0.95, nesterov=True, wd=0.0, ns_steps=5, cap
         W_new = [to_numpy(t, wl.w_dtype) for t in wl.dW]
         M_new = [to_numpy(t, synth.F32) for t in wl.dM]
         u, r = check_step(wl, W_prev, M_prev, W_new, M_new, lr=lr, mu=mu, nesterov=nesterov, wd=wd,
-                          ns_steps=ns_steps, coeffs=coeffs, form=form, sample=sample, tol=tol)
+                          ns_steps=ns_steps, coeffs=coeffs, form=form, sample=sample, tol=tol,
+                          bf16_max_bound=bf16_max_bound)
         worst = (max(worst[0], u), max(worst[1], r))
     return worst
 
@@ -209,7 +224,7 @@ def host_matrix(shape_rc, index, dtype_code, seed, stream, step, sigma):
 
 
 def check_matrix(W_prev, M_prev, G, W_new, M_new, *, w_dtype, g_dtype, lr, mu, nesterov=True, wd=0.0,
-                 ns_steps=5, form="ema", tol=TOL_BF16):
+                 ns_steps=5, form="ema", tol=TOL_BF16, bf16_max_bound=None):
     """Teacher-forced oracle comparison of one logical matrix; returns (ulp, rel)."""
     mu32, omu = oracle_constants(mu, form)
     c32 = tuple(f32(v) for v in oracle.DEFAULT_COEFFS)
@@ -219,8 +234,8 @@ def check_matrix(W_prev, M_prev, G, W_new, M_new, *, w_dtype, g_dtype, lr, mu, n
     ulp = int(ulp_distance(M_new, Mo).max())
     assert ulp <= 1, f"momentum differs by {ulp} ulp"
     if w_dtype == synth.BF16:
-        bf16_weight_check(W_new, Wo, Wp, tol)
-        return ulp, 0.0
+        rel = bf16_weight_check(W_new, Wo, Wp, tol, bf16_max_bound)
+        return ulp, (rel if bf16_max_bound is not None else 0.0)
     rel = rel_fro(widen(W_new, w_dtype) - Wp, Wo - Wp)
     assert rel <= tol, f"rel update error {rel:.3e} > {tol:.2e}"
     return ulp, rel

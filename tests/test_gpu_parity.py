@@ -10,8 +10,8 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import (TOL_BF16, Workload, f32, nsm, oracle_constants, rel_fro, run_steps, to_numpy,
-                      ulp_distance, widen)
+from gpu_util import (TOL_BF16, TOL_BF16_W, Workload, f32, nsm, oracle_constants, rel_fro, run_steps,
+                      to_numpy, torch_from, ulp_distance, widen)
 
 pytestmark = pytest.mark.gpu
 
@@ -91,6 +91,70 @@ def test_options(m, opts):
 def test_bf16_weights_fp32_grads(m):
     wl = Workload([(256, 512), (512, 256)], w_dtype=synth.BF16, g_dtype=synth.F32, g_sigma=1e-3)
     _run(m, wl, steps=2)
+
+
+@pytest.mark.parametrize("g_dtype", [synth.F32, synth.BF16])
+def test_bf16_weights_from_zero_hold_the_update_tolerance(m, g_dtype):
+    # W0 = 0: the bf16 rounding of W_new is at most 2^-8 of the update itself, so
+    # the bound stays within 3.5e-2 of ||dW|| and a 10 % error in the update fails
+    wl = Workload([(256, 512), (512, 256), (130, 700), (700, 130, 2)], w_sigma=0.0, w_dtype=synth.BF16,
+                  g_dtype=g_dtype, g_sigma=1.0 if g_dtype == synth.F32 else 1e-3)
+    ulp, rel = _run(m, wl, bf16_max_bound=TOL_BF16_W)
+    assert ulp <= 1 and rel <= TOL_BF16_W
+
+
+def test_bf16_weights_large_lr_with_decay_hold_the_update_tolerance(m):
+    # W ~ N(0, 0.02) with lr 1 and wd 0.1: the update (about lr * ||U||) dominates
+    # the bf16 rounding of W, and the decay term rides on the old bf16 W
+    wl = Workload([(256, 512), (512, 256), (200, 330, 2)], w_sigma=0.02, w_dtype=synth.BF16, g_sigma=1e-3)
+    ulp, rel = _run(m, wl, lr=1.0, wd=0.1, bf16_max_bound=TOL_BF16_W)
+    assert ulp <= 1 and rel <= TOL_BF16_W
+
+
+def _zero_one_matrix(wl, i, j):
+    # G = M = 0 for matrix j of tensor i, on the host arrays and the device tensors
+    wl.G[i][j] = 0
+    wl.M[i][j] = 0
+    wl.dG[i] = torch_from(wl.G[i], wl.g_dtype)
+    wl.dM[i] = torch_from(wl.M[i], synth.F32)
+
+
+@pytest.mark.parametrize("kernel", ["auto", "gemm"])
+@pytest.mark.parametrize("wd", [0.0, 0.1])
+def test_zero_matrix_in_a_bucket(m, kernel, wd):
+    # an all-zero G and M: V = 0, so X0 = 0 / (0 + eps) = 0 and U = 0; the matrix
+    # keeps its weights (wd = 0) or only decays (wd > 0), with nothing non-finite,
+    # while the other matrices of the same bucket update as usual
+    import torch
+    wl = Workload([(128, 640, 3), (96, 300)], m_sigma=0.02, g_sigma=1e-3)
+    _zero_one_matrix(wl, 0, 1)
+    W0 = wl.dW[0].clone()
+    cfg = m.muon_config_default(ns_kernel=m.MUON_NS_KERNEL_AUTO if kernel == "auto" else m.MUON_NS_KERNEL_GEMM)
+    ulp, rel = _run(m, wl, wd=wd, cfg=cfg)
+    assert ulp <= 1 and rel <= TOL_BF16
+    assert torch.isfinite(wl.dW[0]).all() and torch.isfinite(wl.dM[0]).all()
+    assert int((wl.dM[0][1] != 0).sum()) == 0
+    if wd == 0.0:
+        assert torch.equal(wl.dW[0][1], W0[1])
+    assert not torch.equal(wl.dW[0][0], W0[0]) and not torch.equal(wl.dW[0][2], W0[2])
+
+
+@pytest.mark.parametrize("shape,kernel", [((64, 128), "auto"), ((64, 128), "gemm"), ((200, 330), "auto"),
+                                          ((330, 200), "auto")])
+def test_tiny_norm_where_eps_matters(m, shape, kernel):
+    # ||V||_F ~ 1e-6, so eps = 1e-7 in X0 = V / (||V|| + eps) shrinks every singular
+    # value by ~9 % and moves the update by > 10 % (checked on the oracle here):
+    # the GPU must put eps where the oracle does to stay within 3e-2
+    r, c = shape
+    sigma = 1e-6 / (0.0975 * np.sqrt(r * c))        # EMA + Nesterov from M = 0: V = 0.0975 G
+    wl = Workload([shape], w_sigma=0.0, g_sigma=sigma, g_dtype=synth.F32)
+    V = 0.0975 * wl.G[0][0].astype(np.float64)
+    assert 0.8e-6 < np.linalg.norm(V) < 1.25e-6
+    U_eps, U_none = oracle.newton_schulz(V, eps=1e-7), oracle.newton_schulz(V, eps=0.0)
+    assert rel_fro(U_eps, U_none) > 3 * TOL_BF16
+    cfg = m.muon_config_default(ns_kernel=m.MUON_NS_KERNEL_AUTO if kernel == "auto" else m.MUON_NS_KERNEL_GEMM)
+    ulp, rel = _run(m, wl, cfg=cfg)
+    assert ulp <= 1 and rel <= TOL_BF16
 
 
 def test_per_head_interleaved_qkv_small(m):

@@ -87,6 +87,20 @@ def test_each_product_isolated(m, coeffs, ns_steps):
               cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO))
 
 
+def test_bf16_weights_from_zero_hold_the_update_tolerance(m):
+    # W0 = 0: the bf16 rounding of W_new is at most 2^-8 of the update, so the
+    # bound stays within 3.5e-2 of ||dW|| (the small kernel's per-warp bf16 update)
+    from gpu_util import TOL_BF16_W
+    wl = Workload([(128, 512, 3), (512, 100), (64, 2560, 2)], w_sigma=0.0, w_dtype=synth.BF16, g_sigma=1e-3)
+    k = m.MUON_NS_KERNEL_AUTO
+    _assert_path(m, wl, k, cap=0)
+    ulp, rel = run_steps(m, wl, cfg=_cfg(m, k), cap=0, bf16_max_bound=TOL_BF16_W)
+    assert ulp <= 1 and rel <= TOL_BF16_W
+    wl = Workload([(128, 512, 3), (512, 100)], w_sigma=0.02, w_dtype=synth.BF16, g_sigma=1e-3)
+    ulp, rel = run_steps(m, wl, lr=1.0, wd=0.1, cfg=_cfg(m, k), cap=0, bf16_max_bound=TOL_BF16_W)
+    assert ulp <= 1 and rel <= TOL_BF16_W
+
+
 def test_bf16_weights_and_options(m):
     wl = Workload([(128, 512, 3), (512, 100)], w_dtype=synth.BF16, g_dtype=synth.F32, g_sigma=1e-3)
     run_steps(m, wl, steps=2, wd=0.1, cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO))

@@ -38,7 +38,7 @@ def test_qwen3_4b_layer_full_size(m):
 
 
 def _sampled_step(m, tensors, shapes, plan, samples, *, w_code, g_code, w_sigma, m_sigma, g_sigma, lr=0.02,
-                  mu=0.95):
+                  mu=0.95, bf16_max_bound=None):
     """tensors: list of (W, M, G) device tensors; samples: [(tensor index, matrix index)]."""
     import torch
     pre = {}
@@ -59,7 +59,7 @@ def _sampled_step(m, tensors, shapes, plan, samples, *, w_code, g_code, w_sigma,
     for (ti, j), (W0, M0, G0) in pre.items():
         W, M, _ = tensors[ti]
         _, rel = check_matrix(W0, M0, G0, to_numpy(W[j], w_code), to_numpy(M[j], synth.F32),
-                              w_dtype=w_code, g_dtype=g_code, lr=lr, mu=mu)
+                              w_dtype=w_code, g_dtype=g_code, lr=lr, mu=mu, bf16_max_bound=bf16_max_bound)
         worst = max(worst, rel)
     return worst
 
@@ -123,6 +123,35 @@ def test_moe_experts_48_layers_full_size(m):
                           w_sigma=0.02, m_sigma=0.0, g_sigma=1e-3)
     for W, M, _ in tensors[::17]:
         assert torch.isfinite(W.float()).all() and torch.isfinite(M).all()
+
+
+def test_moe_expert_layer_bf16_weights_from_zero(m):
+    # one layer of the expert workload (384 matrices of 768 x 2048 in the wide form,
+    # buckets of 170, 170 and 44) with bf16 weights starting at 0: the fused bf16
+    # weight update of full 170-matrix buckets, held to 3.5e-2 of ||dW|| (the bf16
+    # rounding of W_new is then at most 2^-8 of the update)
+    from gpu_util import TOL_BF16_W
+    import torch
+    E = 128
+    shapes = [(768, 2048, E), (768, 2048, E), (2048, 768, E)]
+    plan = m.muon_plan([(r, c, k, 0) for (r, c, k) in shapes], bucket_cap_bytes=512 << 20,
+                       config=m.muon_config_default(param_dtype=m.MUON_DTYPE_BF16))
+    info = m.muon_get_plan_info(plan)
+    assert info.n_buckets == 3 and info.max_bucket_matrices == 170
+    m.allocate_workspace(plan)
+    tensors = []
+    for i, (r, c, k) in enumerate(shapes):
+        W = torch.zeros((k, r, c), dtype=torch.bfloat16, device="cuda")
+        M = torch.zeros((k, r, c), dtype=torch.float32, device="cuda")
+        G = device_tensor((k, r, c), synth.BF16, SEED, synth.stream_id(i, synth.ROLE_G), 0, 1e-3)
+        tensors.append((W, M, G))
+    # first and last matrix of each bucket (global matrices [0,170), [170,340), [340,384)), and more
+    samples = [(0, 0), (1, 41), (1, 42), (2, 83), (2, 84), (2, 127), (0, 77), (1, 100), (2, 5)]
+    worst = _sampled_step(m, tensors, shapes, plan, samples, w_code=synth.BF16, g_code=synth.BF16,
+                          w_sigma=0.0, m_sigma=0.0, g_sigma=1e-3, bf16_max_bound=TOL_BF16_W)
+    assert worst <= TOL_BF16_W
+    for W, M, _ in tensors:
+        assert torch.isfinite(W.float()).all() and bool((W != 0).any(dim=(1, 2)).all())
 
 
 def test_offload_full_qwen3_4b_36_layers(m):

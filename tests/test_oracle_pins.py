@@ -224,6 +224,29 @@ def test_apply_update_terms():
     assert np.allclose(out, 2.0 - 0.1 * (math.sqrt(2.0) * 0.5 + 0.3 * 2.0), rtol=0, atol=1e-15)
 
 
+def test_offload_update_on_a_tall_matrix():
+    # the offload writeback U' = sqrt(max(1, rows/cols)) U: a 32 x 8 matrix (rows =
+    # 4 cols) takes the factor 2, its 8 x 32 transpose and a square one take 1; the
+    # singular values of U' of a tall V are 2 p^5(s / (||s|| + eps)) (SVD closed
+    # form); and the host applying W - lr (U' + wd W) lands where apply_update does
+    V = _rand((32, 8), 80)
+    U = oracle.newton_schulz(V)
+    Up = oracle.offload_update(U, 32, 8)
+    assert np.array_equal(Up, 2.0 * U)
+    assert np.array_equal(oracle.offload_update(U.T, 8, 32), U.T)
+    Q = _rand((6, 6), 81)
+    assert np.array_equal(oracle.offload_update(Q, 6, 6), Q)
+    s = np.linalg.svd(V, compute_uv=False)
+    want = 2.0 * _p_iter(s / (math.sqrt(float(np.sum(s ** 2))) + EPS), 5)
+    got = np.linalg.svd(Up, compute_uv=False)
+    assert np.allclose(np.sort(got), np.sort(np.abs(want)), rtol=1e-12, atol=0)
+    W = 0.02 * _rand((32, 8), 82)
+    lr, wd = 0.02, 0.1
+    host = W - lr * (Up + wd * W)
+    assert _rel(host, oracle.apply_update(W, U, lr, wd)) < 1e-15
+    assert _rel(host, W - lr * (2.0 * U + wd * W)) < 1e-15
+
+
 def test_full_step_composes_the_parts():
     W = 0.02 * _rand((5, 8), 70)
     M = 0.02 * _rand((5, 8), 71).astype(np.float32)
