@@ -49,11 +49,17 @@ def ns_flops(rows, cols, steps=None):
     return nominal, algorithmic
 
 
-def ns_executed_flops(rows, cols, steps=None, bm=128, bn=256, bk=64):
-    """Flops the tensor cores execute: whole 128x256 tiles, k rounded up to 64."""
+def ns_executed_flops(rows, cols, steps=None, bm=128, bn=256, bk=64, small=False):
+    """Flops the tensor cores execute.  Grouped GEMMs: whole 128x256 tiles touching
+    the upper triangle (GRAM, POLY) or covering the output (UPDATE), k rounded up to
+    64.  The small-matrix kernel (m <= 128): every product on 128 x 128 tiles, X in
+    128-column chunks (Gram K and UPDATE N rounded up to 128)."""
     steps = NS_STEPS if steps is None else steps
     m, n = min(rows, cols), max(rows, cols)
     cd = lambda a, b: -(-a // b)
+    if small:
+        npad = cd(n, 128) * 128
+        return steps * (2 * 128 * 128 * npad + 2 * 128 ** 3 + 2 * 128 * 128 * npad)
     sym = sum(min(cd(m, bm), (bj * bn + bn - 1) // bm + 1) for bj in range(cd(m, bn)))
     gram = sym * bm * bn * cd(n, bk) * bk * 2
     poly = sym * bm * bn * cd(m, bk) * bk * 2
@@ -134,6 +140,41 @@ def oracle_step(sample):
         oracle.muon_matrix_step(W, M, G, LR, MU, True, WD, NS_STEPS, co)
 
 
+def schedule_config():
+    """The --ns-schedule choice as both arms state it in their config."""
+    if NS_SCHEDULE["kind"] != "minimax":
+        return {"kind": "fixed", "coeffs": [3.4445, -4.7750, 2.0315]}
+    return {"kind": "minimax", "lower": NS_SCHEDULE["lower"], "safety": NS_SCHEDULE["safety"]}
+
+
+def spec_bytes(spec):
+    """Bytes of W, M and G of one step of a workload."""
+    import synth
+    size = {synth.F32: 4, synth.BF16: 2}
+    return sum(k * r * c * (size[spec["w_dtype"]] + 4 + size[spec["g_dtype"]]) for r, c, k in spec["tensors"])
+
+
+def arm_config(spec, world):
+    """The config object of the JSON line, the same for the GPU arm and the reference arm."""
+    elems = sum(k * r * c for r, c, k in spec["tensors"])
+    return {"workload": spec["desc"], "matrices_per_step": sum(k for _, _, k in spec["tensors"]),
+            "elements_per_step": elems, "ns_steps": NS_STEPS, "ns_schedule": schedule_config(),
+            "parallelism": f"replicas{world}",
+            "l2": f"inputs {spec_bytes(spec) / 1e9:.2f} GB per step vs the 129 MB L2"}
+
+
+OFFLOAD_DESC = ("36 Qwen3-4B layers (3.63B Muon parameters) with G bf16 and fp32 M in pinned host memory; "
+                "128 MiB buckets, three staging slots (upload, compute and writeback of three buckets overlap); "
+                "host-blocking step (drained before return)")
+
+
+def offload_config(world, zero_copy=False):
+    return {"workload": OFFLOAD_DESC, "matrices_per_step": 36 * len(QWEN3_4B_LAYER), "ns_steps": NS_STEPS,
+            "ns_schedule": schedule_config(), "parallelism": f"replicas{world}",
+            "offload_mode": "zero-copy (kernels read and write the pinned host buffers)" if zero_copy
+            else "staged (copy engines into device slots)"}
+
+
 def set_schedule(nsm, plan):
     """Applies --ns-schedule to a plan; returns its description for the JSON line."""
     if NS_SCHEDULE["kind"] != "minimax":
@@ -205,20 +246,28 @@ def run_reference(args):
         oracle_step(timed)
     dt = time.perf_counter() - t0
     measured = args.steps * sum(flops[i] for i in picked) / dt          # fp64 flop/s of the oracle
-    work = [(r, c) for (r, c, k) in spec["tensors"] for _ in range(k)]
+    if name == "offload":
+        work = [(r, c) for _ in range(36) for (_, r, c) in QWEN3_4B_LAYER]
+    else:
+        work = [(r, c) for (r, c, k) in spec["tensors"] for _ in range(k)]
     step_s = sum(ns_flops(r, c)[1] for r, c in work) / measured          # one whole workload step
     value = len(work) / step_s
+    sample_ms = 1000 * dt / args.steps
     sample_desc = (f"each timed step runs the oracle on {len(timed)} of the workload's matrices "
                    f"(the cheapest of an evenly spaced sample of {len(sample)}, {per_step:.1f} s per step at "
                    f"most); matrices/s of the whole workload from the measured fp64 flop rate "
                    f"({measured / 1e9:.2f} GFLOP/s of Newton-Schulz work), extrapolated by flop ratio")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * step_s,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sample_ms,
+        "ms_per_step_note": ("wall time of one timed step, i.e. of the oracle on the timed sample; the "
+                             "whole workload's step, extrapolated by flop ratio, is "
+                             "ms_per_step_whole_workload_extrapolated"),
+        "ms_per_step_whole_workload_extrapolated": 1000 * step_s,
+        "matrices_per_timed_step": len(timed),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": spec["desc"] if name != "offload" else name,
-                                        "matrices_per_step": len(work), "ns_steps": NS_STEPS,
-                                        "timed_sample_ms_per_step": 1000 * dt / args.steps},
+        "data": "synthetic",
+        "config": offload_config(world) if name == "offload" else arm_config(spec, world),
         "cpu_baseline": {"value": value, "unit": "matrices/s", "cores": cores_used(), "kind": "oracle",
                          "sample": sample_desc},
         "e2e": {"value": value, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -359,28 +408,47 @@ def hbm_binds(nbytes, flops, hbm_gbs, tensor_tflops):
     return nbytes / (hbm_gbs * 1e9) > flops / (tensor_tflops * 1e12)
 
 
-def roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, ns_bytes, ns_alg_tflops,
+def tf32_peak(bf16_peak):
+    """The 3xTF32 mode's denominator: kind::tf32 products run at half the kind::f16
+    rate per SM on this part (a probe measured 4096 flop/clk/SM against 8192), so
+    the measured bf16 figure times 0.5."""
+    return 0.5 * bf16_peak
+
+
+def roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, executed, ns_bytes,
                    peak_tf, peak_name, peaks, bf16_sustained, traffic):
-    """The roofline object of the Newton-Schulz phase's dominant kernel, per launch."""
+    """The roofline object of the Newton-Schulz phase's dominant kernel, per launch.
+
+    A tensor-bound kernel is measured on the flops its tensor cores execute (whole
+    tiles, the symmetric products' upper tiles only), so ``frac`` cannot pass 1 on
+    work the kernel skips; the algorithmic count (upper-triangle Gram, full A A and
+    B X) is reported beside it.  3xTF32 executes three tf32 products per product."""
     mult = 3 if tf32 else 1
-    tensor_frac = ns_alg_tflops * mult / peak_tf
+    sec = ns_ms * 1e-3
+    exe_tf = executed * mult / sec / 1e12
+    alg_tf = algorithmic * mult / sec / 1e12
     out = {"kernel": ns_kernel_name(nsm, plan, info) + (", 3xTF32" if tf32 else ""),
            "per_launch_ms": ns_ms / ns_launches}
     if hbm_bound:
-        gbs = ns_bytes / (ns_ms * 1e-3) / 1e9
+        gbs = ns_bytes / sec / 1e9
         out.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic,
                     "peak_kind": "measured HBM copy bandwidth",
                     "algorithmic_bytes_per_launch": ns_bytes / ns_launches,
-                    "bytes_counted": "X0 read (bf16) + weights read + weights written",
-                    "tensor_frac": tensor_frac, "tensor_peak_kind": peak_name})
+                    "bytes_counted": "compulsory bytes: inputs read once, weights read and written once",
+                    "tensor_frac": exe_tf / peak_tf, "tensor_frac_algorithmic": alg_tf / peak_tf,
+                    "tensor_peak_kind": peak_name})
     else:
-        out.update({"bound": "tensor", "achieved": ns_alg_tflops * mult, "peak": peak_tf, "unit": "TFLOP/s",
-                    "frac": tensor_frac, "traffic": traffic, "peak_kind": peak_name,
-                    "algorithmic_flops_per_launch": algorithmic / ns_launches})
+        out.update({"bound": "tensor", "achieved": exe_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": exe_tf / peak_tf, "traffic": traffic, "peak_kind": peak_name,
+                    "flops_counted": "executed (whole tiles; upper tiles of X X^T and A A)",
+                    "executed_flops_per_launch": executed * mult / ns_launches,
+                    "achieved_algorithmic": alg_tf, "frac_algorithmic": alg_tf / peak_tf,
+                    "algorithmic_flops_per_launch": algorithmic * mult / ns_launches})
         if not tf32:
-            out["frac_of_burst"] = ns_alg_tflops / peaks["bf16_tflops"]
-            out["frac_of_sustained"] = ns_alg_tflops / bf16_sustained
+            out["frac_of_burst"] = exe_tf / peaks["bf16_tflops"]
+            out["frac_of_sustained"] = exe_tf / bf16_sustained
+            out["frac_algorithmic_of_burst"] = alg_tf / peaks["bf16_tflops"]
     out["traffic_unit"] = "bytes per launch (dram read + write, one ncu capture)"
     return out
 
@@ -495,26 +563,23 @@ def run_gpu(args):
     prep_ms, ns_ms = float(np.median(prep)), float(np.median(nsms))
     nominal = sum(k * ns_flops(r, c)[0] for r, c, k in tensors)
     algorithmic = sum(k * ns_flops(r, c)[1] for r, c, k in tensors)
-    executed = sum(k * ns_executed_flops(r, c) for r, c, k in tensors)
-    elems = sum(k * r * c for r, c, k in tensors)
-    step_bytes = sum(W[i].numel() * W[i].element_size() + M[i].numel() * 4 + G[i].numel() * G[i].element_size()
-                     for i in range(len(tensors)))
+    single_kernel = all(nsm.muon_get_bucket_info(plan, b).ns_single_kernel for b in range(info.n_buckets))
+    executed = sum(k * ns_executed_flops(r, c, small=single_kernel) for r, c, k in tensors)
     prep_bytes = sum(G[i].numel() * (G[i].element_size() + 4 + 4 + 2) for i in range(len(tensors)))
     peaks, peak_kind = load_peaks()
     bf16_sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     peak_tf, peak_name = choose_bf16_peak(peaks, peak_kind, clocks, ms * 1e-3 * args.steps)
     ns_alg_tflops = algorithmic / (ns_ms * 1e-3) / 1e12
     if tf32:
-        # 3xTF32: three kind::tf32 products per product; the tf32 peak is the measured
-        # bf16 figure times the nominal tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)
-        peak_tf = peak_tf * 1.1 / 2.25
-        peak_name = f"{peak_name} x 1.1/2.25 (nominal tf32/bf16); achieved counts the three tf32 products of each product"
+        # 3xTF32: three kind::tf32 products per product, against half the bf16 rate
+        peak_tf = tf32_peak(peak_tf)
+        peak_name = (f"{peak_name} x 0.5 (kind::tf32 measured at half the kind::f16 rate per SM); "
+                     "achieved counts the three tf32 products of each product")
     ns_launches = launches_per_step(nsm, plan, info) - 2 * info.n_buckets
     # the single-launch kernel for m <= 128 reads X0 once and the weights once and
     # writes the weights once (A, B' and the iterations' X stay on chip or in the
     # L2 at best): when those bytes take longer at the HBM peak than the products
     # at the tensor peak, HBM is its roofline
-    single_kernel = all(nsm.muon_get_bucket_info(plan, b).ns_single_kernel for b in range(info.n_buckets))
     ns_bytes = sum(k * min(r, c) * max(r, c) * 2 + 2 * W[i].numel() * W[i].element_size()
                    for i, (r, c, k) in enumerate(tensors))
     hbm_bound = single_kernel and not tf32 and hbm_binds(ns_bytes, algorithmic, peaks["hbm_gbs"], peak_tf)
@@ -590,10 +655,8 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32x3" if tf32 else "bf16", "data": "synthetic",
-        "config": {"workload": spec["desc"], "matrices_per_step": n_mats, "elements_per_step": elems,
-                   "ns_steps": NS_STEPS, "ns_schedule": schedule,
-                   "buckets": int(info.n_buckets), "parallelism": f"replicas{world}",
-                   "l2": f"inputs {step_bytes / 1e9:.2f} GB per step vs the 129 MB L2"},
+        "config": arm_config(spec, world),
+        "plan": {"buckets": int(info.n_buckets), "ns_schedule_detail": schedule},
         "ns_tflops": {"nominal": nominal / (ms * 1e-3) / 1e12, "algorithmic_in_ns_phase": ns_alg_tflops,
                       "executed_in_ns_phase": executed / (ns_ms * 1e-3) / 1e12,
                       "frac_of_sustained_peak_executed": executed / (ns_ms * 1e-3) / 1e12 / bf16_sustained,
@@ -602,8 +665,8 @@ def run_gpu(args):
                      "note": "the weight update runs in the last UPDATE GEMM's epilogue"},
         "elementwise_gbs": {"prep": prep_bytes / (prep_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                             "prep_frac": prep_bytes / (prep_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-        "roofline": roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, ns_bytes,
-                                   ns_alg_tflops, peak_tf, peak_name, peaks, bf16_sustained,
+        "roofline": roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, executed,
+                                   ns_bytes, peak_tf, peak_name, peaks, bf16_sustained,
                                    ns_gemm_traffic() if args.workload == "layer" and not tf32 else None),
         "clocks": clocks,
         "gpu_launches": args.steps * launches_per_step(nsm, plan, info),
@@ -698,14 +761,8 @@ def run_offload(args):
     line = {"metric": METRIC, "value": len(shapes) / (s_ms / 1000), "unit": "matrices/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "36 Qwen3-4B layers (3.63B Muon parameters) with G bf16 and fp32 M in pinned "
-                                   "host memory; 128 MiB buckets, three staging slots (upload, compute and "
-                                   "writeback of three buckets overlap); host-blocking step (drained before "
-                                   "return)",
-                       "buckets": int(info.n_buckets), "matrices_per_step": len(shapes),
-                       "ns_steps": NS_STEPS, "ns_schedule": schedule,
-                       "offload_mode": "zero-copy (kernels read and write the pinned host buffers)" if zero_copy
-                       else "staged (copy engines into device slots)"},
+            "config": offload_config(world, zero_copy),
+            "plan": {"buckets": int(info.n_buckets), "ns_schedule_detail": schedule},
             "host_link": {"h2d_bytes_per_step": hb, "d2h_bytes_per_step": db,
                           "h2d_gbs_avg_over_step": hb / (s_ms * 1e-3) / 1e9,
                           "d2h_gbs_avg_over_step": db / (s_ms * 1e-3) / 1e9,

@@ -58,37 +58,63 @@ def test_hbm_binds_by_time_at_each_peak():
 
 
 def test_tensor_bound_entry():
-    ns_ms, launches, flops = 2.7, 15, 4.6e12
-    tf = flops / (ns_ms * 1e-3) / 1e12
-    r = bench.roofline_entry(_Nsm(0), None, _Info(), False, False, ns_ms, launches, flops, 0, tf,
+    # frac is on executed flops; the algorithmic count is reported beside it
+    ns_ms, launches, flops, executed = 2.7, 15, 4.6e12, 4.35e12
+    tf = executed / (ns_ms * 1e-3) / 1e12
+    r = bench.roofline_entry(_Nsm(0), None, _Info(), False, False, ns_ms, launches, flops, executed, 0,
                              1917.5, "measured bf16 burst", PEAKS, 1719.8, 348.4e6)
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 1917.5
+    assert r["achieved"] == pytest.approx(tf)
     assert r["frac"] == pytest.approx(tf / 1917.5)
     assert r["frac_of_burst"] == pytest.approx(tf / 1917.5)
     assert r["frac_of_sustained"] == pytest.approx(tf / 1719.8)
+    assert r["frac_algorithmic"] == pytest.approx(flops / (ns_ms * 1e-3) / 1e12 / 1917.5)
     assert r["algorithmic_flops_per_launch"] == pytest.approx(flops / launches)
+    assert r["executed_flops_per_launch"] == pytest.approx(executed / launches)
     assert r["per_launch_ms"] == pytest.approx(ns_ms / launches)
     assert r["traffic"] == 348.4e6
 
 
 def test_hbm_bound_entry():
-    ns_ms, nbytes, flops = 2.27, 5.66e9, 1.126e12
-    tf = flops / (ns_ms * 1e-3) / 1e12
-    r = bench.roofline_entry(_Nsm(1), None, _Info(), False, True, ns_ms, 1, flops, nbytes, tf,
+    ns_ms, nbytes, flops, executed = 2.27, 5.66e9, 1.126e12, 1.5e12
+    r = bench.roofline_entry(_Nsm(1), None, _Info(), False, True, ns_ms, 1, flops, executed, nbytes,
                              1917.5, "measured bf16 burst", PEAKS, 1719.8, None)
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6785.2
     assert r["achieved"] == pytest.approx(nbytes / (ns_ms * 1e-3) / 1e9)
     assert r["frac"] == pytest.approx(r["achieved"] / 6785.2)
-    assert r["tensor_frac"] == pytest.approx(tf / 1917.5)
+    assert r["tensor_frac"] == pytest.approx(executed / (ns_ms * 1e-3) / 1e12 / 1917.5)
     assert r["algorithmic_bytes_per_launch"] == nbytes
 
 
-def test_tf32_entry_counts_three_products():
-    ns_ms, launches, flops = 13.2, 15, 4.6e12
-    tf = flops / (ns_ms * 1e-3) / 1e12
-    peak = 1917.5 * 1.1 / 2.25
-    r = bench.roofline_entry(_Nsm(0), None, _Info(), True, False, ns_ms, launches, flops, 0, tf,
-                             peak, "measured bf16 burst x 1.1/2.25", PEAKS, 1719.8, None)
+def test_tf32_entry_counts_three_products_at_half_the_bf16_rate():
+    ns_ms, launches, flops, executed = 13.2, 15, 4.6e12, 4.35e12
+    tf = executed / (ns_ms * 1e-3) / 1e12
+    peak = bench.tf32_peak(1917.5)
+    assert peak == pytest.approx(958.75)
+    r = bench.roofline_entry(_Nsm(0), None, _Info(), True, False, ns_ms, launches, flops, executed, 0,
+                             peak, "measured bf16 burst x 0.5", PEAKS, 1719.8, None)
     assert r["achieved"] == pytest.approx(3 * tf)
     assert r["frac"] == pytest.approx(3 * tf / peak)
     assert "frac_of_burst" not in r
+
+
+def test_executed_flops_of_the_layer_and_the_small_kernel():
+    # layer: executed flops sit below the algorithmic count (POLY runs upper tiles
+    # only) and above the upper-triangle minimum
+    layer = [(4096, 2560), (1024, 2560), (1024, 2560), (2560, 4096), (9728, 2560), (9728, 2560), (2560, 9728)]
+    alg = sum(bench.ns_flops(r, c, 5)[1] for r, c in layer)
+    exe = sum(bench.ns_executed_flops(r, c, 5) for r, c in layer)
+    assert alg == pytest.approx(4.616e12, rel=1e-3)
+    assert 0.9 * alg < exe < alg
+    # a 128 x 2560 head on the small kernel: 128 x 128 tiles, 20 chunks of 128 columns
+    per_it = 2 * 128 * 128 * 2560 * 2 + 2 * 128 ** 3
+    assert bench.ns_executed_flops(128, 2560, 5, small=True) == 5 * per_it
+    assert bench.ns_executed_flops(100, 2500, 1, small=True) == per_it
+
+
+def test_both_arms_state_the_same_config():
+    spec = bench.workload_spec("layer")
+    a, b = bench.arm_config(spec, 1), bench.arm_config(bench.workload_spec("layer"), 1)
+    assert a == b and a["matrices_per_step"] == 7 and a["elements_per_step"] == 100_925_440
+    assert a["l2"].startswith("inputs 1.01 GB")
+    assert bench.offload_config(1)["matrices_per_step"] == 252
