@@ -283,15 +283,19 @@ muon_status muon_get_plan_info(const muon_plan_t* plan, muon_plan_info* info);
 
 /* Defines: as muon_get_plan_info, per bucket.
  * Bucket b: number of matrices, wide-form bf16 bytes, same-shape groups in it,
- * the (m, n) of its first group, and whether its Newton-Schulz iterations run
- * in the single small-matrix kernel (1: every group has m <= 128, bf16
- * arithmetic, ns_kernel AUTO) or as grouped GEMM launches (0). */
+ * the (m, n) of its first group, whether its Newton-Schulz iterations run in the
+ * single small-matrix kernel (1: every group has m <= 128, bf16 arithmetic,
+ * ns_kernel AUTO) or as grouped GEMM launches (0), and whether that kernel also
+ * computes the bucket's momentum in its first pass over each matrix when a step
+ * runs at least one iteration (1: bf16 gradients, every matrix wide, n and the
+ * matrix stride multiples of 8; 0: a separate momentum kernel runs first). */
 typedef struct {
   int64_t n_matrices;
   int64_t bytes;
   int64_t n_groups;
   int64_t m, n;
   int64_t ns_single_kernel;
+  int64_t momentum_in_ns_kernel;
 } muon_bucket_info;
 muon_status muon_get_bucket_info(const muon_plan_t* plan, int64_t b, muon_bucket_info* info);
 

@@ -58,7 +58,8 @@ class muon_plan_info(ctypes.Structure):
 
 class muon_bucket_info(ctypes.Structure):
     _fields_ = [("n_matrices", c_int64), ("bytes", c_int64), ("n_groups", c_int64),
-                ("m", c_int64), ("n", c_int64), ("ns_single_kernel", c_int64)]
+                ("m", c_int64), ("n", c_int64), ("ns_single_kernel", c_int64),
+                ("momentum_in_ns_kernel", c_int64)]
 
 
 class muon_stats(ctypes.Structure):

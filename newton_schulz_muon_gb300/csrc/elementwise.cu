@@ -24,43 +24,13 @@
 
 #include "device.cuh"
 #include "kernels.h"
+#include "momentum.cuh"
 
 namespace muon {
 namespace {
 
 constexpr int kT = kPrepTile;       // 64
 constexpr int kThreads = 256;       // 16 x 16 threads, 4 x 4 elements each
-
-// ---------------------------------------------------------------------------
-// fp32 momentum with the rounding of one correctly rounded operation:
-// mu*m and w*g are split exactly into (high, low) pairs with fma, then added
-// as double-word numbers (Joldes, Muller, Popescu, "Tight and rigorous error
-// bounds for basic building blocks of double-word arithmetic", 2017, accurate
-// DW+DW).  The high word of the result is within 3u^2 relative of the exact
-// value, so it is the nearest float or its neighbour: within 1 ulp.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bp = __fsub_rn(s, a);
-  const float ap = __fsub_rn(s, bp);
-  e = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
-}
-
-__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  e = __fsub_rn(b, __fsub_rn(s, a));
-}
-
-__device__ __forceinline__ float dot2_accurate(float mu, float m, float w, float g) {
-  const float ph = __fmul_rn(mu, m), pl = __fmaf_rn(mu, m, -ph);
-  const float qh = __fmul_rn(w, g), ql = __fmaf_rn(w, g, -qh);
-  float sh, sl, th, tl, vh, vl, zh, zl;
-  two_sum(ph, qh, sh, sl);
-  two_sum(pl, ql, th, tl);
-  fast_two_sum(sh, __fadd_rn(sl, th), vh, vl);
-  fast_two_sum(vh, __fadd_rn(tl, vl), zh, zl);
-  return zh;
-}
 
 struct Tile {
   int seg;
@@ -144,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         mn[j] = dot2_accurate(mu, mo[j], omu, gv[k][j]);
-        v[k][j] = a.nesterov ? __fmaf_rn(mu, mn[j], __fmul_rn(omu, gv[k][j])) : mn[j];
+        v[k][j] = nesterov_input(a.nesterov, mu, mn[j], omu, gv[k][j]);
         sumsq = __fmaf_rn(v[k][j], v[k][j], sumsq);
       }
       mv[k] = make_float4(mn[0], mn[1], mn[2], mn[3]);
@@ -167,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
           const float gj = load_grad(s.g, base + off, a.grad_dtype);
           const float mn = dot2_accurate(mu, mrow[off], omu, gj);
           mrow[off] = mn;
-          v[k][j] = a.nesterov ? __fmaf_rn(mu, mn, __fmul_rn(omu, gj)) : mn;
+          v[k][j] = nesterov_input(a.nesterov, mu, mn, omu, gj);
           sumsq = __fmaf_rn(v[k][j], v[k][j], sumsq);
         }
       }

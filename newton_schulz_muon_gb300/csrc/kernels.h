@@ -155,15 +155,36 @@ struct SmallGroup {
   int32_t pad_[3];
 };
 
+// One run of `count` matrices of one tensor, for the momentum computed inside the
+// small-matrix kernel (bf16 gradients, wide matrices, rows of whole 16-byte units).
+struct SmallPrepSeg {
+  const void* g;         // bf16 gradient of the run's first matrix
+  float* m;              // fp32 momentum of the run's first matrix (updated in place)
+  int64_t stride;        // elements between consecutive matrices in g and m
+  int32_t mat0;          // bucket-local index of the run's first matrix
+  int32_t pad_;
+};
+
 struct SmallArgs {
   SmallGroup g[kMaxGroups];
   int32_t n_groups;
   int32_t n_units;       // matrices in the launch
   int32_t ns_steps;      // quintic iterations (1 .. MUON_MAX_NS_STEPS)
   float coef[16][3];     // iteration k: (a, b, c) of X' = a X + (b A + c A A) X, A = X X^T
-  const float* scale;    // per bucket-local matrix: 1 / (||V||_F + eps), folded into iteration 0
+  float* scale;          // per bucket-local matrix: 1 / (||V||_F + eps), folded into iteration 0
+                         // (written by the kernel when fuse_prep = 1)
   DeviceStatus* status;
   ApplyArgs apply;       // the last iteration applies the weight update (or emits U')
+  // fuse_prep = 1: the kernel's first pass over each matrix computes the momentum
+  // (M updated in place), the Newton-Schulz input V, its Frobenius norm and X0 =
+  // bf16(V) itself, instead of reading X0 written by the momentum kernel
+  int32_t fuse_prep;
+  int32_t nesterov;
+  float mu, omu;         // momentum and its complement (1 for the SGD form)
+  float eps;
+  int32_t n_psegs;
+  int32_t* flags;        // per bucket-local matrix: 1 if the norm was not finite (fuse_prep)
+  SmallPrepSeg pseg[kMaxSegs];
 };
 
 // GEMM tile shape (bf16): 128 x 256 outputs per CTA, 64-deep k blocks.

@@ -42,6 +42,15 @@
 //     caller's tensor (columns of U for tall matrices).
 //   * The first iteration folds the normalisation s = 1/(||V||_F + eps) into its
 //     epilogues (Gram: s^2, UPDATE: s), as the grouped kernel does.
+//   * With fuse_prep (bf16 gradients, wide matrices) the first pass over a matrix
+//     is also its momentum step ("Muon Optimizer + FSDP", section 背景: M_t =
+//     momentum_update(grad) feeds NewtonSchulz): the epilogue warps, idle until
+//     the Gram of iteration 0 is done, stream G and M through the shared memory
+//     that A, B' and the X' tiles use later, write M_new back, write X0 =
+//     bf16(V) to the workspace (for the UPDATE of iteration 0) and into the ring
+//     stage the MMA warp builds the Gram from, and sum V^2 for the norm.  G and
+//     M are read once, and X0 does not make a round trip through HBM between two
+//     kernels.
 //
 // Roles (one persistent CTA per SM, 576 threads; matrices u = blockIdx.x,
 // blockIdx.x + gridDim.x, ...):
@@ -69,6 +78,7 @@
 #include "device.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "momentum.cuh"
 
 namespace muon {
 namespace {
@@ -90,6 +100,17 @@ static_assert(kXsBufs * kChunk <= kXsRegion, "X' tiles fit in the shared region"
 constexpr uint32_t kOffRing = kOffXS + kXsRegion;
 static_assert(kOffRing % 1024 == 0, "ring stages are 1024-byte aligned");
 constexpr size_t kSmemS = kOffRing + (size_t)kStagesS * kChunk + 1024;
+// fused momentum: 32-column quarters of a chunk staged in the region of A, B' and
+// the X' tiles (free while a matrix's first pass runs): G 128 rows x 64 bytes,
+// then M 128 rows x 128 bytes, per slot; three quarters in flight
+constexpr uint32_t kPrepThreads = kEpiWarps * 32;
+constexpr int kPrepCols = 32;
+constexpr uint32_t kPrepG = 128u * 64u;                // 8 KB
+constexpr uint32_t kPrepSlot = kPrepG + 128u * 128u;   // 24 KB
+constexpr int kPrepSlots = 4;
+static_assert(kPrepSlots * kPrepSlot <= kOffRing, "the staging slots fit below the ring");
+static_assert(kChunkCols == 4 * kPrepCols, "four quarters per chunk");
+constexpr uint32_t kPrepBar = 1;                       // named barrier of the epilogue warps
 constexpr uint32_t kTmemColsS = 512;
 constexpr uint32_t kColG = 0, kColU = 128;            // UPDATE buffer u at kColU + 128 u
 constexpr uint32_t kColP = kColU;                     // A A, drained before any UPDATE of the iteration
@@ -295,6 +316,148 @@ struct UnitRef {
   int g, b;
 };
 
+// The momentum run holding bucket-local matrix `mat`.
+__device__ __forceinline__ const SmallPrepSeg& prep_seg(const SmallArgs& a, int mat) {
+  int lo = 0, hi = a.n_psegs - 1;
+  while (lo < hi) {  // last run with mat0 <= mat
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.pseg[mid].mat0 <= mat) lo = mid; else hi = mid - 1;
+  }
+  return a.pseg[lo];
+}
+
+// The first pass over matrix `mat` (fuse_prep), by the kPrepThreads epilogue
+// threads together.  Per 32-column quarter q of each 128-column chunk: G (bf16)
+// and M (fp32) are copied into staging slot q % 4 with cp.async, three quarters
+// ahead; then each thread takes 8 consecutive elements of one row:
+//   M_new = mu M + w G (within 1 ulp), V = mu M_new + w G (Nesterov) or M_new,
+// stores M_new in place and X0 = bf16(V) in the workspace, writes bf16(V) into
+// the chunk's ring stage (128-byte swizzle, the layout the TMA loads give; rows
+// >= m and columns >= n zero) and adds V^2 to its sum.  A complete stage is
+// handed to the MMA warp on its full barrier; after the last one the producer is
+// told that X0 is in the workspace (prep_done).  Returns the matrix's s = 1 /
+// (||V||_F + eps) and whether the norm was finite; false when a wait was
+// abandoned (every epilogue thread returns the same).  `pos` is the ring
+// position of the matrix's first chunk, advanced past the chunks filled here.
+// Staging layout: G row r at r * 64 bytes (16-byte unit u at u * 16); M row r at
+// r * 128 bytes with its 16-byte unit u at (u ^ (r & 1)) * 16, so that the eight
+// lanes of a shared-memory phase (two rows) hit distinct banks.
+__device__ __forceinline__ bool prep_matrix(const SmallArgs& a, const SmallGroup& G, int b, int mat, uint8_t* smem,
+                                            uint8_t* ring, uint64_t* full_bar, uint64_t* empty_bar,
+                                            uint64_t* prep_done, float* norm_red, uint32_t& pos,
+                                            volatile int* abort_p, unsigned* status, float& s_out, bool& bad_out) {
+  const int et = (int)threadIdx.x - 64;  // 0 .. kPrepThreads - 1
+  const int lane = threadIdx.x & 31;
+  const SmallPrepSeg& P = prep_seg(a, mat);
+  const int64_t moff = (int64_t)(mat - P.mat0) * P.stride;
+  const __nv_bfloat16* gmat = reinterpret_cast<const __nv_bfloat16*>(P.g) + moff;
+  float* mmat = P.m + moff;
+  __nv_bfloat16* xmat = reinterpret_cast<__nv_bfloat16*>(G.x) + (int64_t)b * G.mstride;
+  const int m = G.m, n = G.n;
+  const int64_t ld = G.ld;
+  const int q_end = 4 * ((n + kChunkCols - 1) / kChunkCols);
+  const float mu = a.mu, omu = a.omu;
+  auto issue = [&](int q) {
+    if (q < q_end) {
+      uint8_t* sg = smem + (size_t)(q & (kPrepSlots - 1)) * kPrepSlot;
+      uint8_t* sm = sg + kPrepG;
+      const int c0 = q * kPrepCols;
+      {
+        const int row = et >> 2, u = et & 3, c = c0 + 8 * u;
+        if (row < m && c < n) cp_async_16(sg + row * 64 + u * 16, gmat + (int64_t)row * n + c);
+      }
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int i = it * (int)kPrepThreads + et;
+        const int row = i >> 3, u = i & 7, c = c0 + 4 * u;
+        if (row < m && c < n) cp_async_16(sm + row * 128 + ((u ^ (row & 1)) << 4), mmat + (int64_t)row * n + c);
+      }
+    }
+    cp_async_commit();  // possibly empty: every thread counts the same groups
+  };
+  // (the caller has synchronised the epilogue threads: the staging region was the
+  // previous matrix's A, B' and weight-update buffers)
+  issue(0);
+  issue(1);
+  issue(2);
+  const int row = et >> 2, cg = et & 3;
+  float sumsq = 0.f;
+  for (int q = 0; q < q_end; ++q) {
+    cp_async_wait<2>();  // this thread's copies of quarter q have landed
+    const uint32_t stage = pos % (uint32_t)kStagesS, lap = (pos / (uint32_t)kStagesS) & 1u;
+    if ((q & 3) == 0) {
+      // the chunk's ring stage has been read by the MMAs of its previous use
+      bool got = true;
+      if (lane == 0) got = mbar_wait(&empty_bar[stage], lap ^ 1u, abort_p, status);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!bar_and(kPrepBar, kPrepThreads, got)) {
+        cp_async_wait<0>();
+        return false;
+      }
+    } else {
+      __syncwarp();
+      bar_sync(kPrepBar, kPrepThreads);  // everyone's copies of q are visible; slot (q + 3) % 4 is free
+    }
+    issue(q + 3);
+    const uint8_t* sg = smem + (size_t)(q & (kPrepSlots - 1)) * kPrepSlot;
+    const uint8_t* sm = sg + kPrepG;
+    const int c = q * kPrepCols + 8 * cg;
+    float v[8];
+    if (row < m && c < n) {
+      float g[8];
+      unpack8(*reinterpret_cast<const uint4*>(sg + row * 64 + cg * 16), g);
+      const float4 m0 = *reinterpret_cast<const float4*>(sm + row * 128 + (((2 * cg) ^ (row & 1)) << 4));
+      const float4 m1 = *reinterpret_cast<const float4*>(sm + row * 128 + (((2 * cg + 1) ^ (row & 1)) << 4));
+      const float mo[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      float mn[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        mn[e] = dot2_accurate(mu, mo[e], omu, g[e]);
+        v[e] = nesterov_input(a.nesterov, mu, mn[e], omu, g[e]);
+        sumsq = __fmaf_rn(v[e], v[e], sumsq);
+      }
+      float* mp = mmat + (int64_t)row * n + c;
+      __stcs(reinterpret_cast<float4*>(mp), make_float4(mn[0], mn[1], mn[2], mn[3]));
+      __stcs(reinterpret_cast<float4*>(mp + 4), make_float4(mn[4], mn[5], mn[6], mn[7]));
+      *reinterpret_cast<uint4*>(xmat + (int64_t)row * ld + c) = pack8(v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = 0.f;
+    }
+    uint8_t* st = ring + (size_t)stage * kChunk + (size_t)((q >> 1) & 1) * kTile;
+    *reinterpret_cast<uint4*>(st + sw128(row, (q & 1) * 4 + cg)) = pack8(v);
+    if ((q & 3) == 3) {
+      fence_proxy_async_shared();  // the stage is read by the tensor core
+      fence_proxy_async_global();  // X0 is read by the producer's TMA loads
+      __syncwarp();
+      bar_sync(kPrepBar, kPrepThreads);
+      if (et == 0) {
+        mbar_arrive(&full_bar[stage]);
+        if (q + 1 == q_end) mbar_arrive(prep_done);
+      }
+      ++pos;
+    }
+  }
+  cp_async_wait<0>();
+  // ||V||_F^2: per-thread fp32 sums, warp sums, then the 16 warps in a fixed order in fp64
+  const float w = warp_sum(sumsq);
+  if (lane == 0) norm_red[et >> 5] = w;
+  __syncwarp();
+  bar_sync(kPrepBar, kPrepThreads);
+  double tot = 0.0;
+#pragma unroll
+  for (int i = 0; i < (int)kEpiWarps; ++i) tot += (double)norm_red[i];
+  const bool finite = isfinite(tot);
+  s_out = finite ? (float)(1.0 / (sqrt(tot) + (double)a.eps)) : 0.f;
+  bad_out = !finite;
+  if (et == 0) {
+    a.scale[mat] = s_out;
+    a.flags[mat] = finite ? 0 : 1;
+    if (!finite) atomicAdd(&a.status->nonfinite, 1u);
+  }
+  return true;
+}
+
 __device__ __forceinline__ UnitRef decode_unit(const SmallArgs& a, int u) {
   int g = 0;
   for (int i = 1; i < a.n_groups; ++i)
@@ -330,6 +493,8 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
   __shared__ __align__(8) uint64_t xs_full[kXsBufs];     // X' tile written (epilogue warps)
   __shared__ __align__(8) uint64_t xs_empty[kXsBufs];    // X' tile read by the Gram (MMA commit) and the store
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t prep_done;            // fused momentum: X0 of the matrix is in the workspace
+  __shared__ float norm_red[kEpiWarps];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -357,6 +522,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
       mbar_init(&xs_empty[i], 2);
     }
     mbar_init(&drain_bar, 1);
+    mbar_init(&prep_done, 1);
     abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -382,6 +548,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
     int stage = 0;
     uint32_t phase = 0;
     uint32_t xc = 0;  // X' tiles stored so far
+    uint32_t pd = 0;  // prep_done phase
     bool ok = true;
     // X is read again every iteration: keep its lines in L2 ahead of streams
     const uint64_t keep = l2_policy_evict_last();
@@ -404,6 +571,15 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         // those the previous pass wrote last, the likeliest to be still in L2
         const bool rev = pass & 1;
         auto chunk = [&](int j) { return rev ? nch - 1 - j : j; };
+        if (pass == 0 && a.fuse_prep) {
+          // the epilogue warps fill these stages with X0 computed from G and M;
+          // UPDATE 0 reads X0 back once all of it is in the workspace
+          ring_advance(stage, phase, nch);
+          const bool got = mbar_wait(&prep_done, pd, abort_p, status);
+          pd ^= 1u;
+          if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+          continue;
+        }
         if (pass == 0 || pass == K) {  // no X' to store: plain loads
           for (int j = 0; j < nch; ++j) {
             const bool got = mbar_wait(&empty_bar[stage], phase ^ 1u, abort_p, status);
@@ -630,13 +806,31 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
     uint8_t* ab = smem + kOffAB + (size_t)box * kTile;    // this warp's box of A / B
     float* wbuf = reinterpret_cast<float*>(smem + kOffXS + (size_t)ew * kWarpBuf);
     uint32_t gp = 0, pp = 0, uc = 0, xc = 0;
+    uint32_t pos = 0;  // ring position (fused momentum fills the first pass's stages)
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+      if (a.fuse_prep) {
+        // every epilogue thread arrives here for every matrix (done with the
+        // previous one's shared memory), and a warp that gave up a wait stops
+        // them all together: the named barriers below are then never left waiting
+        __syncwarp();
+        ok = bar_and(kPrepBar, kPrepThreads, ok);
+      }
+      if (!ok) break;
       const UnitRef t = decode_unit(a, u);
       const SmallGroup& G = a.g[t.g];
       const int nch = (G.n + kChunkCols - 1) / kChunkCols;
       const int mat = G.mat_base + t.b;
-      const float s = a.scale[mat];
+      float s;
+      bool bad = false;
+      if (a.fuse_prep) {
+        ok = prep_matrix(a, G, t.b, mat, smem, ring, full_bar, empty_bar, &prep_done, norm_red, pos, abort_p,
+                         status, s, bad);
+        if (!ok) break;
+        pos += (uint32_t)(nch * K);  // the UPDATE passes' stages, filled by the producer
+      } else {
+        s = a.scale[mat];
+      }
       for (int k = 0; ok && k < K; ++k) {
         // ---- A = (s^2 in iteration 0) X X^T, bf16, into shared memory ----
         ok = __all_sync(0xffffffffu, mbar_wait(&gram_full, gp, abort_p, status));
@@ -691,6 +885,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         bool vec = false;
         if (last) {
           tg = apply_target(a.apply, mat);
+          if (a.fuse_prep) tg.skip = !a.apply.emit && a.apply.skip_nonfinite && bad;
           vec = piece_vec(a.apply, tg);
         }
         for (int j = 0; j < nch; ++j) {

@@ -548,6 +548,22 @@ bool uses_small_kernel(const muon_config& c, const Bucket& b) {
   return c.ns_precision == MUON_NS_BF16 && c.ns_kernel == MUON_NS_KERNEL_AUTO && small_bucket(b);
 }
 
+// Whether the small-matrix kernel computes the bucket's momentum in its first pass
+// instead of the momentum kernel: bf16 gradients, every matrix wide (no transpose),
+// and rows of G and M that are whole 16-byte units at 16-byte aligned offsets
+// (n and the matrix stride multiples of 8 elements).
+bool fuses_momentum(const muon_plan_t* p, const Bucket& b, int ns_steps) {
+  if (ns_steps <= 0 || !uses_small_kernel(p->cfg, b) || p->cfg.grad_dtype != MUON_DTYPE_BF16) return false;
+  for (const BGroup& g : b.groups) {
+    if (g.n % 8 != 0) return false;
+    for (const Run& r : g.runs) {
+      const TensorInfo& t = p->tensors[r.tensor];
+      if (t.transposed || t.stride % 8 != 0) return false;
+    }
+  }
+  return true;
+}
+
 // Every iteration of a small-matrix bucket in one launch (X updated in place in
 // the workspace's first X buffer), the weight update fused into the last one.
 // (a, b, c) of Newton-Schulz iteration k: the plan's schedule (its last triple
@@ -568,7 +584,7 @@ static_assert(sizeof(SmallArgs::coef) / sizeof(SmallArgs::coef[0]) == MUON_MAX_N
               "one coefficient triple per possible iteration");
 
 muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st,
-                             const ApplyArgs& fused) {
+                             const ApplyArgs& fused, const PrepArgs* prep) {
   SmallArgs sa;
   std::memset(&sa, 0, sizeof(sa));
   std::vector<size_t> order(b.groups.size());
@@ -597,16 +613,33 @@ muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cuda
   sa.scale = at<float>(p, p->off_scale);
   sa.status = at<DeviceStatus>(p, p->off_status);
   sa.apply = fused;
+  if (prep) {  // the momentum of the bucket, computed in the kernel's first pass
+    sa.fuse_prep = 1;
+    sa.nesterov = prep->nesterov;
+    sa.mu = prep->mu;
+    sa.omu = prep->omu;
+    sa.eps = prep->eps;
+    sa.flags = prep->flags;
+    sa.n_psegs = prep->n_segs;
+    for (int i = 0; i < prep->n_segs; ++i) {
+      sa.pseg[i].g = prep->seg[i].g;
+      sa.pseg[i].m = prep->seg[i].m;
+      sa.pseg[i].stride = prep->seg[i].stride;
+      sa.pseg[i].mat0 = prep->seg[i].mat0;
+    }
+  }
   cudaError_t e = launch_ns_small(sa, p->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "small-matrix Newton-Schulz launch");
   return MUON_OK;
 }
 
+// `prep`: the bucket's momentum arguments when the small-matrix kernel computes the
+// momentum itself (fuses_momentum), else null (the momentum kernel has run).
 muon_status enqueue_ns(muon_plan_t* p, const Bucket& b, int ns_steps, cudaStream_t st,
-                       const ApplyArgs* fused = nullptr) {
+                       const ApplyArgs* fused = nullptr, const PrepArgs* prep = nullptr) {
   const muon_config& c = p->cfg;
   const bool tf32 = c.ns_precision == MUON_NS_TF32X3;
-  if (fused && ns_steps > 0 && uses_small_kernel(c, b)) return enqueue_ns_small(p, b, ns_steps, st, *fused);
+  if (fused && ns_steps > 0 && uses_small_kernel(c, b)) return enqueue_ns_small(p, b, ns_steps, st, *fused, prep);
   LaunchShape shapes[3];
   for (int mode = kGram; mode <= kUpdate; ++mode) shapes[mode] = launch_shape(b, mode, tf32);
   for (int it = 0; it < ns_steps; ++it) {
@@ -819,6 +852,7 @@ muon_status muon_get_bucket_info(const muon_plan_t* plan, int64_t b, muon_bucket
   info->m = k.groups[0].m;
   info->n = k.groups[0].n;
   info->ns_single_kernel = uses_small_kernel(plan->cfg, k) ? 1 : 0;
+  info->momentum_in_ns_kernel = fuses_momentum(plan, k, 1) ? 1 : 0;
   return MUON_OK;
 }
 
@@ -991,16 +1025,20 @@ muon_status muon_step(muon_plan_t* p, void* const* params, const void* const* gr
     };
     PrepArgs pa;
     make_prep_args(p, b, ptrs, mu, nesterov, pa);
+    const bool fuse = fuses_momentum(p, b, ns_steps);
     if (timing) cudaEventRecord(p->events[bi].start, st);
-    cudaError_t e = launch_prep(pa, st);
-    if (e != cudaSuccess) return cuda_fail(e, "momentum_prep launch");
-    e = launch_norm(pa, st);
-    if (e != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
+    cudaError_t e;
+    if (!fuse) {
+      e = launch_prep(pa, st);
+      if (e != cudaSuccess) return cuda_fail(e, "momentum_prep launch");
+      e = launch_norm(pa, st);
+      if (e != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
+    }
     if (timing) cudaEventRecord(p->events[bi].prep, st);
     // the weight update runs in the last UPDATE's epilogue; with no iteration, in its own kernel
     ApplyArgs aa;
     make_apply_args(p, b, ptrs, ns_steps & 1, lr, wd, 0, ns_steps, aa);
-    muon_status s = enqueue_ns(p, b, ns_steps, st, ns_steps > 0 ? &aa : nullptr);
+    muon_status s = enqueue_ns(p, b, ns_steps, st, ns_steps > 0 ? &aa : nullptr, fuse ? &pa : nullptr);
     if (s != MUON_OK) return s;
     if (timing) cudaEventRecord(p->events[bi].ns, st);
     if (ns_steps == 0) {
@@ -1186,12 +1224,15 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
     };
     PrepArgs pa;
     make_prep_args(p, b, stage_ptrs, mu, nesterov, pa);
+    const bool fuse = fuses_momentum(p, b, ns_steps);
     if (timing) cudaEventRecord(p->events[bi].prep, cs);  // marks compute start for this bucket
-    if ((e = launch_prep(pa, cs)) != cudaSuccess) return cuda_fail(e, "momentum_prep launch");
-    if ((e = launch_norm(pa, cs)) != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
+    if (!fuse) {
+      if ((e = launch_prep(pa, cs)) != cudaSuccess) return cuda_fail(e, "momentum_prep launch");
+      if ((e = launch_norm(pa, cs)) != cudaSuccess) return cuda_fail(e, "norm_finalize launch");
+    }
     ApplyArgs aa;
     make_apply_args(p, b, stage_ptrs, ns_steps & 1, 0.f, 0.f, 1, ns_steps, aa);
-    muon_status s = enqueue_ns(p, b, ns_steps, cs, ns_steps > 0 ? &aa : nullptr);
+    muon_status s = enqueue_ns(p, b, ns_steps, cs, ns_steps > 0 ? &aa : nullptr, fuse ? &pa : nullptr);
     if (s != MUON_OK) return s;
     if (timing) cudaEventRecord(p->events[bi].ns, cs);
     if (ns_steps == 0 && (e = launch_apply(aa, cs)) != cudaSuccess) return cuda_fail(e, "emit launch");

@@ -119,14 +119,15 @@ def _zero_one_matrix(wl, i, j):
     wl.dM[i] = torch_from(wl.M[i], synth.F32)
 
 
-@pytest.mark.parametrize("kernel", ["auto", "gemm"])
+@pytest.mark.parametrize("kernel,last", [("auto", 304), ("auto", 300), ("gemm", 300)])
 @pytest.mark.parametrize("wd", [0.0, 0.1])
-def test_zero_matrix_in_a_bucket(m, kernel, wd):
+def test_zero_matrix_in_a_bucket(m, kernel, last, wd):
     # an all-zero G and M: V = 0, so X0 = 0 / (0 + eps) = 0 and U = 0; the matrix
     # keeps its weights (wd = 0) or only decays (wd > 0), with nothing non-finite,
-    # while the other matrices of the same bucket update as usual
+    # while the other matrices of the same bucket update as usual.  With n = 304 the
+    # small kernel computes the momentum itself; with 300 the momentum kernel does.
     import torch
-    wl = Workload([(128, 640, 3), (96, 300)], m_sigma=0.02, g_sigma=1e-3)
+    wl = Workload([(128, 640, 3), (96, last)], m_sigma=0.02, g_sigma=1e-3)
     _zero_one_matrix(wl, 0, 1)
     W0 = wl.dW[0].clone()
     cfg = m.muon_config_default(ns_kernel=m.MUON_NS_KERNEL_AUTO if kernel == "auto" else m.MUON_NS_KERNEL_GEMM)
@@ -139,16 +140,18 @@ def test_zero_matrix_in_a_bucket(m, kernel, wd):
     assert not torch.equal(wl.dW[0][0], W0[0]) and not torch.equal(wl.dW[0][2], W0[2])
 
 
-@pytest.mark.parametrize("shape,kernel", [((64, 128), "auto"), ((64, 128), "gemm"), ((200, 330), "auto"),
-                                          ((330, 200), "auto")])
-def test_tiny_norm_where_eps_matters(m, shape, kernel):
+@pytest.mark.parametrize("shape,kernel,g_dtype", [((64, 128), "auto", synth.F32), ((64, 128), "auto", synth.BF16),
+                                                  ((64, 128), "gemm", synth.F32), ((200, 330), "auto", synth.F32),
+                                                  ((330, 200), "auto", synth.F32)])
+def test_tiny_norm_where_eps_matters(m, shape, kernel, g_dtype):
     # ||V||_F ~ 1e-6, so eps = 1e-7 in X0 = V / (||V|| + eps) shrinks every singular
     # value by ~9 % and moves the update by > 10 % (checked on the oracle here):
-    # the GPU must put eps where the oracle does to stay within 3e-2
+    # the GPU must put eps where the oracle does to stay within 3e-2 (bf16
+    # gradients: the small kernel computes the norm itself)
     r, c = shape
     sigma = 1e-6 / (0.0975 * np.sqrt(r * c))        # EMA + Nesterov from M = 0: V = 0.0975 G
-    wl = Workload([shape], w_sigma=0.0, g_sigma=sigma, g_dtype=synth.F32)
-    V = 0.0975 * wl.G[0][0].astype(np.float64)
+    wl = Workload([shape], w_sigma=0.0, g_sigma=sigma, g_dtype=g_dtype)
+    V = 0.0975 * widen(wl.G[0][0], g_dtype)
     assert 0.8e-6 < np.linalg.norm(V) < 1.25e-6
     U_eps, U_none = oracle.newton_schulz(V, eps=1e-7), oracle.newton_schulz(V, eps=0.0)
     assert rel_fro(U_eps, U_none) > 3 * TOL_BF16

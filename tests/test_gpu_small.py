@@ -61,6 +61,95 @@ def test_small_kernel_matches_oracle(m, shapes, kernel):
     assert ulp <= 1 and rel <= TOL_BF16
 
 
+def _assert_momentum_fused(m, wl, want, cap=512 << 20):
+    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=_cfg(m, m.MUON_NS_KERNEL_AUTO))
+    info = m.muon_get_plan_info(plan)
+    got = [m.muon_get_bucket_info(plan, b).momentum_in_ns_kernel for b in range(info.n_buckets)]
+    assert got == [want] * info.n_buckets
+
+
+# The small kernel computes the momentum itself in its first pass over each matrix
+# (bf16 gradients, wide matrices, n a multiple of 8): G and M staged 32 columns at
+# a time, M written back, X0 into the ring stage and the workspace, the norm summed
+# in the kernel.  Momentum within 1 ulp and updates within 3e-2 of the oracle.
+@pytest.mark.parametrize("shapes", [
+    [(128, 2560, 4)],                 # per-head shape: 20 whole chunks
+    [(100, 704), (3, 8)],             # m < 128 (rows zero in the ring), n = 5.5 chunks; one 8-column row block
+    [(128, 136, 2), (1, 64)],         # one chunk and one quarter; a single row
+    [(64, 4104)],                     # n above 4096, a last chunk of 8 columns
+    [(96, 256, 3), (32, 512, 2), (128, 128), (16, 1024, 5)],   # four groups in one launch
+])
+def test_fused_momentum_matches_oracle(m, shapes):
+    wl = Workload(shapes, m_sigma=0.02, g_sigma=1e-3)
+    _assert_path(m, wl, m.MUON_NS_KERNEL_AUTO)
+    _assert_momentum_fused(m, wl, 1)
+    ulp, rel = run_steps(m, wl, steps=3, cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO))
+    assert ulp <= 1 and rel <= TOL_BF16
+
+
+@pytest.mark.parametrize("opts", [dict(form="sgd"), dict(nesterov=False), dict(wd=0.1, mu=0.5),
+                                  dict(ns_steps=1), dict(ns_steps=6)])
+def test_fused_momentum_options(m, opts):
+    wl = Workload([(128, 640, 3), (64, 1000 + 24)], m_sigma=0.02, g_sigma=1e-3)
+    _assert_momentum_fused(m, wl, 1)
+    ulp, rel = run_steps(m, wl, steps=2, cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO), **opts)
+    assert ulp <= 1 and rel <= TOL_BF16
+
+
+def test_fused_momentum_more_matrices_than_ctas(m):
+    # 400 + 3 matrices: each CTA runs the fused first pass for several matrices in turn
+    wl = Workload([(16, 208, 400), (128, 304, 3)], m_sigma=0.02, g_sigma=1e-3)
+    _assert_momentum_fused(m, wl, 1, cap=0)
+    ulp, rel = run_steps(m, wl, steps=2, cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO), cap=0)
+    assert ulp <= 1 and rel <= TOL_BF16
+
+
+def test_fused_momentum_nonfinite_matrix_is_skipped(m):
+    import torch
+    wl = Workload([(64, 128, 3), (32, 256)], m_sigma=0.02, g_sigma=1e-3)
+    _assert_momentum_fused(m, wl, 1)
+    W0 = [t.clone() for t in wl.dW]
+    g = wl.dG[0].clone()
+    g[1, 5, 7] = float("nan")
+    plan = m.muon_plan(wl.plan_shapes())
+    m.allocate_workspace(plan)
+    m.muon_step(plan, wl.dW, [g, wl.dG[1]], wl.dM, 0.02, 0.95, True, 0.0, 5)
+    st, nf = m.muon_sync(plan)
+    assert st == m.MUON_WARN_NONFINITE and nf == 1
+    assert torch.equal(wl.dW[0][1], W0[0][1])
+    assert not torch.equal(wl.dW[0][0], W0[0][0]) and not torch.equal(wl.dW[1], W0[1])
+    assert torch.isfinite(wl.dW[0]).all() and torch.isfinite(wl.dW[1]).all()
+
+
+def test_fused_and_separate_momentum_agree(m):
+    # one set of bf16 gradients given twice: as bf16 (the small kernel computes the
+    # momentum) and widened to fp32 (the momentum kernel runs first, as for any fp32
+    # gradient).  Both round the same fp32 operations, so the new momentum is
+    # bit-identical; the updates differ only through the order of the norm's sums.
+    import torch
+    outs = []
+    for fused in (True, False):
+        wl = Workload([(128, 2560, 3), (64, 512)], m_sigma=0.02, g_sigma=1e-3)
+        cfg = _cfg(m, m.MUON_NS_KERNEL_AUTO)
+        if not fused:
+            cfg.grad_dtype = m.MUON_DTYPE_F32
+            wl.dG = [g.float() for g in wl.dG]
+        plan = m.muon_plan(wl.plan_shapes(), config=cfg)
+        assert m.muon_get_bucket_info(plan, 0).momentum_in_ns_kernel == int(fused)
+        m.allocate_workspace(plan)
+        W0 = [w.clone() for w in wl.dW]
+        m.muon_step(plan, wl.dW, wl.dG, wl.dM, 0.02, 0.95, True, 0.0, 5)
+        assert m.muon_sync(plan) == (m.MUON_OK, 0)
+        torch.cuda.synchronize()
+        outs.append(([w - w0 for w, w0 in zip(wl.dW, W0)], [x.clone() for x in wl.dM]))
+    (dw_f, m_f), (dw_s, m_s) = outs
+    for a, b in zip(m_f, m_s):
+        assert torch.equal(a, b)
+    for a, b in zip(dw_f, dw_s):
+        for j in range(a.shape[0]):
+            assert rel_fro(a[j].double().cpu().numpy(), b[j].double().cpu().numpy()) <= 1e-2
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_more_matrices_than_ctas(m, kernel):
     # 400 + 3 matrices in one launch: each CTA takes several, of two groups
