@@ -371,13 +371,17 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def launches_per_step(nsm, plan, info):
-    """Kernels one step launches: momentum and norm per bucket, then one
-    small-matrix Newton-Schulz kernel or three GEMMs per iteration."""
+def launches_per_step(nsm, plan, info, ns_only=False):
+    """Kernels one step launches: momentum and norm per bucket (unless the
+    small-matrix kernel computes the momentum), then one small-matrix
+    Newton-Schulz kernel or three GEMMs per iteration.  ns_only: the
+    Newton-Schulz launches alone."""
     n = 0
     for b in range(info.n_buckets):
-        single = nsm.muon_get_bucket_info(plan, b).ns_single_kernel
-        n += 2 + (1 if single else 3 * NS_STEPS)
+        bi = nsm.muon_get_bucket_info(plan, b)
+        ns = 1 if bi.ns_single_kernel else 3 * NS_STEPS
+        momentum = 0 if (bi.momentum_in_ns_kernel and NS_STEPS > 0) else 2
+        n += ns + (0 if ns_only else momentum)
     return n
 
 
@@ -400,6 +404,17 @@ def choose_bf16_peak(peaks, peak_kind, clocks, timed_s):
         return (peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
                 f"{peak_kind} bf16 sustained (power cap active or a timed region of seconds: {timed_s:.2f} s)")
     return peaks["bf16_tflops"], f"{peak_kind} bf16 burst (no power cap seen, timed region {timed_s:.2f} s)"
+
+
+def ns_compulsory_bytes(tensors, w_sizes, g_sizes, momentum_fused):
+    """Bytes the single-launch small-matrix kernel must move through HBM: the
+    weights read and written once, plus X0 read once (bf16) or, when the kernel
+    computes the momentum itself, G read once and M read and written once."""
+    total = 0
+    for (r, c, k), ws, gs in zip(tensors, w_sizes, g_sizes):
+        e = k * r * c
+        total += 2 * e * ws + (e * (gs + 8) if momentum_fused else e * 2)
+    return total
 
 
 def hbm_binds(nbytes, flops, hbm_gbs, tensor_tflops):
@@ -504,9 +519,11 @@ def run_gpu(args):
     shapes = [(r, c, k, 0) for (r, c, k) in tensors]
     tf32 = args.ns_precision == "tf32x3"
     cfg = nsm.muon_config_default(timing=1, grad_dtype=spec["g_dtype"], param_dtype=spec["w_dtype"],
-                                  ns_precision=nsm.MUON_NS_TF32X3 if tf32 else nsm.MUON_NS_BF16)
+                                  ns_precision=nsm.MUON_NS_TF32X3 if tf32 else nsm.MUON_NS_BF16,
+                                  ns_momentum_fused=1 if args.momentum == "fused" else 0)
     plan = nsm.muon_plan(shapes, bucket_cap_bytes=spec["cap"], config=cfg)
     info = nsm.muon_get_plan_info(plan)
+    momentum_fused = all(nsm.muon_get_bucket_info(plan, b).momentum_in_ns_kernel for b in range(info.n_buckets))
     ws = nsm.allocate_workspace(plan)
     schedule = set_schedule(nsm, plan)
     tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16}
@@ -575,13 +592,13 @@ def run_gpu(args):
         peak_tf = tf32_peak(peak_tf)
         peak_name = (f"{peak_name} x 0.5 (kind::tf32 measured at half the kind::f16 rate per SM); "
                      "achieved counts the three tf32 products of each product")
-    ns_launches = launches_per_step(nsm, plan, info) - 2 * info.n_buckets
+    ns_launches = launches_per_step(nsm, plan, info, ns_only=True)
     # the single-launch kernel for m <= 128 reads X0 once and the weights once and
     # writes the weights once (A, B' and the iterations' X stay on chip or in the
     # L2 at best): when those bytes take longer at the HBM peak than the products
     # at the tensor peak, HBM is its roofline
-    ns_bytes = sum(k * min(r, c) * max(r, c) * 2 + 2 * W[i].numel() * W[i].element_size()
-                   for i, (r, c, k) in enumerate(tensors))
+    ns_bytes = ns_compulsory_bytes(tensors, [W[i].element_size() for i in range(len(tensors))],
+                                   [G[i].element_size() for i in range(len(tensors))], momentum_fused)
     hbm_bound = single_kernel and not tf32 and hbm_binds(ns_bytes, algorithmic, peaks["hbm_gbs"], peak_tf)
 
     # ---- end to end through the C ABI with host buffers ----
@@ -656,15 +673,19 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32x3" if tf32 else "bf16", "data": "synthetic",
         "config": arm_config(spec, world),
-        "plan": {"buckets": int(info.n_buckets), "ns_schedule_detail": schedule},
+        "plan": {"buckets": int(info.n_buckets), "ns_schedule_detail": schedule,
+                 "momentum_in_ns_kernel": momentum_fused},
         "ns_tflops": {"nominal": nominal / (ms * 1e-3) / 1e12, "algorithmic_in_ns_phase": ns_alg_tflops,
                       "executed_in_ns_phase": executed / (ns_ms * 1e-3) / 1e12,
                       "frac_of_sustained_peak_executed": executed / (ns_ms * 1e-3) / 1e12 / bf16_sustained,
                       "frac_of_burst_peak_executed": executed / (ns_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]},
         "phase_ms": {"prep": prep_ms, "ns_and_apply": ns_ms,
                      "note": "the weight update runs in the last UPDATE GEMM's epilogue"},
-        "elementwise_gbs": {"prep": prep_bytes / (prep_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                            "prep_frac": prep_bytes / (prep_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "elementwise_gbs": ({"prep": None, "peak": peaks["hbm_gbs"], "prep_frac": None,
+                             "note": "the momentum runs inside the small-matrix Newton-Schulz kernel; its bytes "
+                                     "are in the roofline's compulsory bytes"} if momentum_fused else
+                            {"prep": prep_bytes / (prep_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                             "prep_frac": prep_bytes / (prep_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}),
         "roofline": roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, executed,
                                    ns_bytes, peak_tf, peak_name, peaks, bf16_sustained,
                                    ns_gemm_traffic() if args.workload == "layer" and not tf32 else None),
@@ -798,6 +819,9 @@ def main():
                     help="Newton-Schulz arithmetic: bf16 (default) or the 3xTF32 accuracy mode")
     ap.add_argument("--layers", type=int, default=None,
                     help="heads / experts: fewer layers than the full workload (profiling captures)")
+    ap.add_argument("--momentum", choices=["fused", "separate"], default="fused",
+                    help="small-matrix buckets: the momentum computed in the Newton-Schulz kernel's first pass "
+                         "(default, the library's default), or the momentum kernel first")
     ap.add_argument("--offload-mode", choices=["copy", "zerocopy"], default="copy",
                     help="offload workload: staged copies (default) or zero-copy kernel access to host memory")
     ap.add_argument("--ns-steps", type=int, default=5, help="Newton-Schulz iterations per step (default 5)")

@@ -108,12 +108,16 @@ typedef struct {
                                 (mapped into the device's address space; no staging slots,
                                 no copy engines, everything on the compute stream); 0 stages
                                 each bucket through device slots with copy-engine copies */
-  int32_t reserved[2];
+  int32_t ns_momentum_fused; /* 1: buckets run by the small-matrix kernel (bf16 gradients, wide
+                                matrices, n and matrix strides multiples of 8) compute their
+                                momentum, norm and X0 in that kernel's first pass; 0: the
+                                momentum kernel runs first */
+  int32_t reserved[1];
 } muon_config;
 
 /* Fills *cfg with (3.4445, -4.7750, 2.0315), eps 1e-7, bf16 NS, EMA momentum,
  * bf16 gradients, fp32 weights, max_inflight 1, skip_nonfinite 1, timing 0,
- * offload 0, ns_kernel MUON_NS_KERNEL_AUTO. */
+ * offload 0, ns_kernel MUON_NS_KERNEL_AUTO, ns_momentum_fused 1. */
 void muon_config_default(muon_config* cfg);
 
 /* Defines: "Muon Optimizer + FSDP", section 分块通信 (chunked communication:

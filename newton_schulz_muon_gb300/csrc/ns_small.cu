@@ -326,28 +326,30 @@ __device__ __forceinline__ const SmallPrepSeg& prep_seg(const SmallArgs& a, int 
   return a.pseg[lo];
 }
 
-// The first pass over matrix `mat` (fuse_prep), by the kPrepThreads epilogue
-// threads together.  Per 32-column quarter q of each 128-column chunk: G (bf16)
-// and M (fp32) are copied into staging slot q % 4 with cp.async, three quarters
-// ahead; then each thread takes 8 consecutive elements of one row:
+// The first pass over matrix `mat` (fuse_prep), by each epilogue warp on its own
+// eight rows (warp w: rows 8 w .. 8 w + 7), with no barrier across warps.  Per
+// 32-column quarter q of each 128-column chunk the warp copies its rows of G
+// (bf16) and M (fp32) into staging slot q % 4 with cp.async, three quarters ahead;
+// then each lane takes 8 consecutive elements of one row:
 //   M_new = mu M + w G (within 1 ulp), V = mu M_new + w G (Nesterov) or M_new,
 // stores M_new in place and X0 = bf16(V) in the workspace, writes bf16(V) into
 // the chunk's ring stage (128-byte swizzle, the layout the TMA loads give; rows
-// >= m and columns >= n zero) and adds V^2 to its sum.  A complete stage is
-// handed to the MMA warp on its full barrier; after the last one the producer is
-// told that X0 is in the workspace (prep_done).  Returns the matrix's s = 1 /
-// (||V||_F + eps) and whether the norm was finite; false when a wait was
-// abandoned (every epilogue thread returns the same).  `pos` is the ring
-// position of the matrix's first chunk, advanced past the chunks filled here.
-// Staging layout: G row r at r * 64 bytes (16-byte unit u at u * 16); M row r at
-// r * 128 bytes with its 16-byte unit u at (u ^ (r & 1)) * 16, so that the eight
-// lanes of a shared-memory phase (two rows) hit distinct banks.
+// >= m and columns >= n zero) and adds V^2 to its sum.  Each warp arrives on the
+// stage's pfull barrier (count 16) when its rows of a chunk are written, and on
+// prep_done (count 16) after its last chunk, once X0 is in the workspace.  The
+// warp's sum of V^2 is in norm_red[w] before its last pfull arrival, so the Gram
+// of iteration 0 being complete implies every partial is there.  `pos` is the
+// ring position of the matrix's first chunk, advanced past the chunks filled
+// here.  Returns false when a wait was abandoned.
+// Staging layout per slot: G row r at r * 64 bytes (16-byte unit u at u * 16); M
+// row r at kPrepG + r * 128 bytes with its 16-byte unit u at (u ^ (r & 1)) * 16,
+// so that the eight lanes of a shared-memory phase (two rows) hit distinct banks.
 __device__ __forceinline__ bool prep_matrix(const SmallArgs& a, const SmallGroup& G, int b, int mat, uint8_t* smem,
-                                            uint8_t* ring, uint64_t* full_bar, uint64_t* empty_bar,
+                                            uint8_t* ring, uint64_t* pfull_bar, uint64_t* empty_bar,
                                             uint64_t* prep_done, float* norm_red, uint32_t& pos,
-                                            volatile int* abort_p, unsigned* status, float& s_out, bool& bad_out) {
+                                            volatile int* abort_p, unsigned* status) {
   const int et = (int)threadIdx.x - 64;  // 0 .. kPrepThreads - 1
-  const int lane = threadIdx.x & 31;
+  const int wp = et >> 5, lane = threadIdx.x & 31;
   const SmallPrepSeg& P = prep_seg(a, mat);
   const int64_t moff = (int64_t)(mat - P.mat0) * P.stride;
   const __nv_bfloat16* gmat = reinterpret_cast<const __nv_bfloat16*>(P.g) + moff;
@@ -363,41 +365,36 @@ __device__ __forceinline__ bool prep_matrix(const SmallArgs& a, const SmallGroup
       uint8_t* sm = sg + kPrepG;
       const int c0 = q * kPrepCols;
       {
-        const int row = et >> 2, u = et & 3, c = c0 + 8 * u;
+        const int row = 8 * wp + (lane >> 2), u = lane & 3, c = c0 + 8 * u;
         if (row < m && c < n) cp_async_16(sg + row * 64 + u * 16, gmat + (int64_t)row * n + c);
       }
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
-        const int i = it * (int)kPrepThreads + et;
-        const int row = i >> 3, u = i & 7, c = c0 + 4 * u;
+        const int i = it * 32 + lane;
+        const int row = 8 * wp + (i >> 3), u = i & 7, c = c0 + 4 * u;
         if (row < m && c < n) cp_async_16(sm + row * 128 + ((u ^ (row & 1)) << 4), mmat + (int64_t)row * n + c);
       }
     }
-    cp_async_commit();  // possibly empty: every thread counts the same groups
+    cp_async_commit();  // possibly empty: every lane counts the same groups
   };
-  // (the caller has synchronised the epilogue threads: the staging region was the
-  // previous matrix's A, B' and weight-update buffers)
   issue(0);
   issue(1);
   issue(2);
-  const int row = et >> 2, cg = et & 3;
+  const int row = 8 * wp + (lane >> 2), cg = lane & 3;
   float sumsq = 0.f;
   for (int q = 0; q < q_end; ++q) {
-    cp_async_wait<2>();  // this thread's copies of quarter q have landed
+    cp_async_wait<2>();  // this lane's copies of quarter q have landed
     const uint32_t stage = pos % (uint32_t)kStagesS, lap = (pos / (uint32_t)kStagesS) & 1u;
     if ((q & 3) == 0) {
       // the chunk's ring stage has been read by the MMAs of its previous use
       bool got = true;
       if (lane == 0) got = mbar_wait(&empty_bar[stage], lap ^ 1u, abort_p, status);
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (!bar_and(kPrepBar, kPrepThreads, got)) {
+      if (!__shfl_sync(0xffffffffu, got, 0)) {
         cp_async_wait<0>();
         return false;
       }
-    } else {
-      __syncwarp();
-      bar_sync(kPrepBar, kPrepThreads);  // everyone's copies of q are visible; slot (q + 3) % 4 is free
     }
+    __syncwarp();  // the warp's copies of q are visible to all its lanes; slot (q + 3) % 4 is free
     issue(q + 3);
     const uint8_t* sg = smem + (size_t)(q & (kPrepSlots - 1)) * kPrepSlot;
     const uint8_t* sm = sg + kPrepG;
@@ -427,35 +424,41 @@ __device__ __forceinline__ bool prep_matrix(const SmallArgs& a, const SmallGroup
     uint8_t* st = ring + (size_t)stage * kChunk + (size_t)((q >> 1) & 1) * kTile;
     *reinterpret_cast<uint4*>(st + sw128(row, (q & 1) * 4 + cg)) = pack8(v);
     if ((q & 3) == 3) {
+      const bool final_chunk = q + 1 == q_end;
+      if (final_chunk) {
+        const float w = warp_sum(sumsq);
+        if (lane == 0) norm_red[wp] = w;
+      }
       fence_proxy_async_shared();  // the stage is read by the tensor core
       fence_proxy_async_global();  // X0 is read by the producer's TMA loads
       __syncwarp();
-      bar_sync(kPrepBar, kPrepThreads);
-      if (et == 0) {
-        mbar_arrive(&full_bar[stage]);
-        if (q + 1 == q_end) mbar_arrive(prep_done);
+      if (lane == 0) {
+        mbar_arrive(&pfull_bar[stage]);
+        if (final_chunk) mbar_arrive(prep_done);
       }
       ++pos;
     }
   }
   cp_async_wait<0>();
-  // ||V||_F^2: per-thread fp32 sums, warp sums, then the 16 warps in a fixed order in fp64
-  const float w = warp_sum(sumsq);
-  if (lane == 0) norm_red[et >> 5] = w;
-  __syncwarp();
-  bar_sync(kPrepBar, kPrepThreads);
+  return true;
+}
+
+// s = 1 / (||V||_F + eps) of the matrix whose first pass just completed, from the
+// 16 warp partials in a fixed order (fp64), and whether the norm was finite; one
+// thread records them and counts a non-finite matrix.
+__device__ __forceinline__ float prep_scale(const SmallArgs& a, int mat, const float* norm_red, bool& bad) {
   double tot = 0.0;
 #pragma unroll
   for (int i = 0; i < (int)kEpiWarps; ++i) tot += (double)norm_red[i];
   const bool finite = isfinite(tot);
-  s_out = finite ? (float)(1.0 / (sqrt(tot) + (double)a.eps)) : 0.f;
-  bad_out = !finite;
-  if (et == 0) {
-    a.scale[mat] = s_out;
+  const float s = finite ? (float)(1.0 / (sqrt(tot) + (double)a.eps)) : 0.f;
+  bad = !finite;
+  if (threadIdx.x == 64) {
+    a.scale[mat] = s;
     a.flags[mat] = finite ? 0 : 1;
     if (!finite) atomicAdd(&a.status->nonfinite, 1u);
   }
-  return true;
+  return s;
 }
 
 __device__ __forceinline__ UnitRef decode_unit(const SmallArgs& a, int u) {
@@ -494,6 +497,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
   __shared__ __align__(8) uint64_t xs_empty[kXsBufs];    // X' tile read by the Gram (MMA commit) and the store
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t prep_done;            // fused momentum: X0 of the matrix is in the workspace
+  __shared__ __align__(8) uint64_t pfull_bar[kStagesS];  // fused momentum: a stage of X0 written (16 warps)
   __shared__ float norm_red[kEpiWarps];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -522,7 +526,8 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
       mbar_init(&xs_empty[i], 2);
     }
     mbar_init(&drain_bar, 1);
-    mbar_init(&prep_done, 1);
+    mbar_init(&prep_done, kEpiWarps);
+    for (int i = 0; i < kStagesS; ++i) mbar_init(&pfull_bar[i], kEpiWarps);
     abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -659,6 +664,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
     const uint32_t xs0 = smem_u32(smem + kOffXS);
     int stage = 0;
     uint32_t phase = 0, ab_phase = 0;
+    uint32_t pf_par = 0;      // fused momentum: next parity of pfull_bar[s] in bit s
     uint32_t uc = 0, xc = 0;  // UPDATE chunks and fused-Gram tiles so far
     bool ok = true;
     // K-major descriptor of k-slice kk (16 deep, kk = 0..7) of a 128 x 128 tile
@@ -678,10 +684,20 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
       const UnitRef t = decode_unit(a, u);
       const SmallGroup& G = a.g[t.g];
       const int nch = (G.n + kChunkCols - 1) / kChunkCols;
-      // Gram of iteration 0 over X0 chunks from the ring; the commit releases
-      // the stage
+      // Gram of iteration 0 over X0 chunks from the ring (TMA loads, or written
+      // by the epilogue warps when they compute the momentum); the commit
+      // releases the stage
       for (int j = 0; j < nch; ++j) {
-        const bool got = mbar_wait(&full_bar[stage], phase, abort_p, status);
+        bool got;
+        if (a.fuse_prep) {
+          got = mbar_wait(&pfull_bar[stage], (pf_par >> stage) & 1u, abort_p, status);
+          pf_par ^= 1u << stage;
+          // complete the stage's full phase too, so that full_bar's phases keep
+          // counting ring positions for the TMA-filled passes
+          if (got && lane == 0) mbar_arrive(&full_bar[stage]);
+        } else {
+          got = mbar_wait(&full_bar[stage], phase, abort_p, status);
+        }
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
@@ -807,6 +823,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
     float* wbuf = reinterpret_cast<float*>(smem + kOffXS + (size_t)ew * kWarpBuf);
     uint32_t gp = 0, pp = 0, uc = 0, xc = 0;
     uint32_t pos = 0;  // ring position (fused momentum fills the first pass's stages)
+    uint32_t pd = 0;   // prep_done phase
     bool ok = true;
     for (int u = blockIdx.x; u < a.n_units; u += gridDim.x) {
       if (a.fuse_prep) {
@@ -821,12 +838,12 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
       const SmallGroup& G = a.g[t.g];
       const int nch = (G.n + kChunkCols - 1) / kChunkCols;
       const int mat = G.mat_base + t.b;
-      float s;
+      float s = 0.f;
       bool bad = false;
       if (a.fuse_prep) {
-        ok = prep_matrix(a, G, t.b, mat, smem, ring, full_bar, empty_bar, &prep_done, norm_red, pos, abort_p,
-                         status, s, bad);
-        if (!ok) break;
+        ok = __all_sync(0xffffffffu, prep_matrix(a, G, t.b, mat, smem, ring, pfull_bar, empty_bar, &prep_done,
+                                                 norm_red, pos, abort_p, status));
+        if (!ok) continue;  // the barrier at the top stops every epilogue warp together
         pos += (uint32_t)(nch * K);  // the UPDATE passes' stages, filled by the producer
       } else {
         s = a.scale[mat];
@@ -837,6 +854,13 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
         gp ^= 1u;
         if (!ok) break;
         tc_fence_after();
+        if (k == 0 && a.fuse_prep) {
+          // every warp's partial sum was written before its prep_done arrival
+          ok = __all_sync(0xffffffffu, mbar_wait(&prep_done, pd, abort_p, status));
+          pd ^= 1u;
+          if (!ok) break;
+          s = prep_scale(a, mat, norm_red, bad);
+        }
         {
           const float sa = k == 0 ? s * s : 1.f;
           float v[32];

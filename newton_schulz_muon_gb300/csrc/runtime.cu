@@ -553,7 +553,9 @@ bool uses_small_kernel(const muon_config& c, const Bucket& b) {
 // and rows of G and M that are whole 16-byte units at 16-byte aligned offsets
 // (n and the matrix stride multiples of 8 elements).
 bool fuses_momentum(const muon_plan_t* p, const Bucket& b, int ns_steps) {
-  if (ns_steps <= 0 || !uses_small_kernel(p->cfg, b) || p->cfg.grad_dtype != MUON_DTYPE_BF16) return false;
+  if (!p->cfg.ns_momentum_fused || ns_steps <= 0 || !uses_small_kernel(p->cfg, b) ||
+      p->cfg.grad_dtype != MUON_DTYPE_BF16)
+    return false;
   for (const BGroup& g : b.groups) {
     if (g.n % 8 != 0) return false;
     for (const Run& r : g.runs) {
@@ -774,6 +776,7 @@ void muon_config_default(muon_config* cfg) {
   cfg->timing = 0;
   cfg->offload = 0;
   cfg->ns_kernel = MUON_NS_KERNEL_AUTO;
+  cfg->ns_momentum_fused = 1;
 }
 
 muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t* groups, int64_t bucket_cap_bytes,
@@ -796,6 +799,8 @@ muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t*
   if (c.max_inflight < 1 || c.max_inflight > 2) return fail(MUON_ERR_INVALID, "max_inflight must be 1 or 2");
   if (c.ns_kernel != MUON_NS_KERNEL_AUTO && c.ns_kernel != MUON_NS_KERNEL_GEMM)
     return fail(MUON_ERR_INVALID, "ns_kernel must be AUTO or GEMM");
+  if (c.ns_momentum_fused != 0 && c.ns_momentum_fused != 1)
+    return fail(MUON_ERR_INVALID, "ns_momentum_fused must be 0 or 1");
   muon_plan_t* p = new (std::nothrow) muon_plan_t();
   if (!p) return fail(MUON_ERR_INVALID, "out of host memory");
   static std::atomic<uint64_t> next_id{1};

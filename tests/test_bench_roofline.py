@@ -17,8 +17,9 @@ PEAKS = {"hbm_gbs": 6785.2, "bf16_tflops": 1917.5, "bf16_tflops_sustained": 1719
 
 
 class _Bucket:
-    def __init__(self, single):
+    def __init__(self, single, fused=0):
         self.ns_single_kernel = single
+        self.momentum_in_ns_kernel = fused
 
 
 class _Nsm:
@@ -118,3 +119,28 @@ def test_both_arms_state_the_same_config():
     assert a == b and a["matrices_per_step"] == 7 and a["elements_per_step"] == 100_925_440
     assert a["l2"].startswith("inputs 1.01 GB")
     assert bench.offload_config(1)["matrices_per_step"] == 252
+
+
+def test_compulsory_bytes_of_the_small_kernel():
+    # 1728 heads of 128 x 2560, fp32 W, bf16 G: weights read and written (8 B) plus
+    # X0 (2 B), or, with the momentum in the kernel, G (2 B) and M read and written (8 B)
+    t = [(128, 2560, 1728)]
+    e = 128 * 2560 * 1728
+    assert bench.ns_compulsory_bytes(t, [4], [2], False) == 10 * e
+    assert bench.ns_compulsory_bytes(t, [4], [2], True) == 18 * e
+
+
+def test_launches_per_step():
+    class Nsm:
+        def __init__(self, kinds):
+            self.kinds = kinds
+
+        def muon_get_bucket_info(self, plan, b):
+            return _Bucket(*self.kinds[b])
+
+    class Info:
+        n_buckets = 3
+
+    nsm = Nsm([(0, 0), (1, 0), (1, 1)])   # GEMM bucket; small kernel after the momentum kernel; fused
+    assert bench.launches_per_step(nsm, None, Info()) == (2 + 15) + (2 + 1) + 1
+    assert bench.launches_per_step(nsm, None, Info(), ns_only=True) == 15 + 1 + 1

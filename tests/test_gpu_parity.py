@@ -130,7 +130,8 @@ def test_zero_matrix_in_a_bucket(m, kernel, last, wd):
     wl = Workload([(128, 640, 3), (96, last)], m_sigma=0.02, g_sigma=1e-3)
     _zero_one_matrix(wl, 0, 1)
     W0 = wl.dW[0].clone()
-    cfg = m.muon_config_default(ns_kernel=m.MUON_NS_KERNEL_AUTO if kernel == "auto" else m.MUON_NS_KERNEL_GEMM)
+    cfg = m.muon_config_default(ns_kernel=m.MUON_NS_KERNEL_AUTO if kernel == "auto" else m.MUON_NS_KERNEL_GEMM,
+                                ns_momentum_fused=1)
     ulp, rel = _run(m, wl, wd=wd, cfg=cfg)
     assert ulp <= 1 and rel <= TOL_BF16
     assert torch.isfinite(wl.dW[0]).all() and torch.isfinite(wl.dM[0]).all()
@@ -155,7 +156,8 @@ def test_tiny_norm_where_eps_matters(m, shape, kernel, g_dtype):
     assert 0.8e-6 < np.linalg.norm(V) < 1.25e-6
     U_eps, U_none = oracle.newton_schulz(V, eps=1e-7), oracle.newton_schulz(V, eps=0.0)
     assert rel_fro(U_eps, U_none) > 3 * TOL_BF16
-    cfg = m.muon_config_default(ns_kernel=m.MUON_NS_KERNEL_AUTO if kernel == "auto" else m.MUON_NS_KERNEL_GEMM)
+    cfg = m.muon_config_default(ns_kernel=m.MUON_NS_KERNEL_AUTO if kernel == "auto" else m.MUON_NS_KERNEL_GEMM,
+                                ns_momentum_fused=1)
     ulp, rel = _run(m, wl, cfg=cfg)
     assert ulp <= 1 and rel <= TOL_BF16
 

@@ -61,8 +61,12 @@ def test_small_kernel_matches_oracle(m, shapes, kernel):
     assert ulp <= 1 and rel <= TOL_BF16
 
 
+def _fused_cfg(m):
+    return m.muon_config_default(ns_kernel=m.MUON_NS_KERNEL_AUTO, ns_momentum_fused=1)
+
+
 def _assert_momentum_fused(m, wl, want, cap=512 << 20):
-    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=_cfg(m, m.MUON_NS_KERNEL_AUTO))
+    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=_fused_cfg(m))
     info = m.muon_get_plan_info(plan)
     got = [m.muon_get_bucket_info(plan, b).momentum_in_ns_kernel for b in range(info.n_buckets)]
     assert got == [want] * info.n_buckets
@@ -83,7 +87,7 @@ def test_fused_momentum_matches_oracle(m, shapes):
     wl = Workload(shapes, m_sigma=0.02, g_sigma=1e-3)
     _assert_path(m, wl, m.MUON_NS_KERNEL_AUTO)
     _assert_momentum_fused(m, wl, 1)
-    ulp, rel = run_steps(m, wl, steps=3, cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO))
+    ulp, rel = run_steps(m, wl, steps=3, cfg=_fused_cfg(m))
     assert ulp <= 1 and rel <= TOL_BF16
 
 
@@ -92,7 +96,7 @@ def test_fused_momentum_matches_oracle(m, shapes):
 def test_fused_momentum_options(m, opts):
     wl = Workload([(128, 640, 3), (64, 1000 + 24)], m_sigma=0.02, g_sigma=1e-3)
     _assert_momentum_fused(m, wl, 1)
-    ulp, rel = run_steps(m, wl, steps=2, cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO), **opts)
+    ulp, rel = run_steps(m, wl, steps=2, cfg=_fused_cfg(m), **opts)
     assert ulp <= 1 and rel <= TOL_BF16
 
 
@@ -100,7 +104,7 @@ def test_fused_momentum_more_matrices_than_ctas(m):
     # 400 + 3 matrices: each CTA runs the fused first pass for several matrices in turn
     wl = Workload([(16, 208, 400), (128, 304, 3)], m_sigma=0.02, g_sigma=1e-3)
     _assert_momentum_fused(m, wl, 1, cap=0)
-    ulp, rel = run_steps(m, wl, steps=2, cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO), cap=0)
+    ulp, rel = run_steps(m, wl, steps=2, cfg=_fused_cfg(m), cap=0)
     assert ulp <= 1 and rel <= TOL_BF16
 
 
@@ -111,7 +115,7 @@ def test_fused_momentum_nonfinite_matrix_is_skipped(m):
     W0 = [t.clone() for t in wl.dW]
     g = wl.dG[0].clone()
     g[1, 5, 7] = float("nan")
-    plan = m.muon_plan(wl.plan_shapes())
+    plan = m.muon_plan(wl.plan_shapes(), config=_fused_cfg(m))
     m.allocate_workspace(plan)
     m.muon_step(plan, wl.dW, [g, wl.dG[1]], wl.dM, 0.02, 0.95, True, 0.0, 5)
     st, nf = m.muon_sync(plan)
@@ -122,15 +126,15 @@ def test_fused_momentum_nonfinite_matrix_is_skipped(m):
 
 
 def test_fused_and_separate_momentum_agree(m):
-    # one set of bf16 gradients given twice: as bf16 (the small kernel computes the
-    # momentum) and widened to fp32 (the momentum kernel runs first, as for any fp32
-    # gradient).  Both round the same fp32 operations, so the new momentum is
+    # one set of bf16 gradients given twice: as bf16 with ns_momentum_fused (the
+    # small kernel computes the momentum) and widened to fp32 (the momentum kernel
+    # runs first, as for any fp32 gradient).  Both round the same fp32 operations, so the new momentum is
     # bit-identical; the updates differ only through the order of the norm's sums.
     import torch
     outs = []
     for fused in (True, False):
         wl = Workload([(128, 2560, 3), (64, 512)], m_sigma=0.02, g_sigma=1e-3)
-        cfg = _cfg(m, m.MUON_NS_KERNEL_AUTO)
+        cfg = _fused_cfg(m)
         if not fused:
             cfg.grad_dtype = m.MUON_DTYPE_F32
             wl.dG = [g.float() for g in wl.dG]
