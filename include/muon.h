@@ -213,6 +213,11 @@ muon_status muon_step(muon_plan_t* plan, void* const* params, const void* const*
  * buckets are in writeback while one computes.  The host then applies
  * W -= lr * (U' + wd * W) itself.  Blocks until every writeback has landed
  * (the host reads the results next) or timeout_ms passes (MUON_ERR_TIMEOUT).
+ * After MUON_ERR_TIMEOUT (or an error once some work was enqueued) the step's
+ * device work is still in flight and keeps writing h_momentum and h_update_out:
+ * the host must not read or reuse them before synchronising the device, or
+ * before a later muon_offload_step of the plan returns MUON_OK (each step waits
+ * for the previous step's writebacks before it touches the host buffers).
  *   h_grads / h_momentum / h_update_out [n_mats]: pinned host pointers laid out
  *   like the device tensors of muon_step.  MUON_ERR_NOT_PINNED if any is not
  *   page-locked. */
@@ -220,6 +225,19 @@ muon_status muon_offload_step(muon_plan_t* plan, const void* const* h_grads,
                               void* const* h_momentum, void* const* h_update_out,
                               int64_t n_mats, float mu, int32_t nesterov, int32_t ns_steps,
                               void* compute, void* copy, int64_t timeout_ms);
+
+/* Defines: DeepSpeed PR "[Muon] CPU offload: pin the momentum and overlap the
+ * host writeback", section Changes (writebacks drained before the host reads);
+ * the injection itself is this library's, for testing the failure path on the
+ * host without faulting a device.
+ * Makes the `nth` host-link copy (0-based, in enqueue order: per bucket the
+ * gradient and momentum uploads, then the momentum and update writebacks) of the
+ * plan's next muon_offload_step report a failure instead of being enqueued, as if
+ * cudaMemcpy2DAsync had returned an error: that step returns MUON_ERR_CUDA after
+ * enqueueing the work before it, and the injection is cleared.  nth = -1 clears
+ * it.  Work already enqueued still completes; the plan's next offload step waits
+ * for it.  Pure host state.  Errors: MUON_ERR_INVALID (NULL plan, nth < -1). */
+muon_status muon_inject_copy_failure(muon_plan_t* plan, int64_t nth);
 
 /* muon_step for callers that cannot allocate device memory: code running inside
  * an allocator or memory-pool callback (which must not re-enter the allocator),

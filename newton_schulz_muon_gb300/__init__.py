@@ -98,6 +98,7 @@ def _load() -> ctypes.CDLL:
         "muon_step_noalloc": (c_int32, [P, POINTER(P), POINTER(P), POINTER(P), c_int64, c_float, c_float,
                                         c_int32, c_float, c_int32, P]),
         "muon_noalloc_scratch_bytes": (c_size_t, []),
+        "muon_inject_copy_failure": (c_int32, [P, c_int64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -223,6 +224,12 @@ def muon_step_noalloc(plan: Plan, params, grads, momentum, lr: float, mu: float,
                                     float(lr), float(mu), int(bool(nesterov)), float(wd), int(ns_steps),
                                     _stream_ptr(stream)),
            "muon_step_noalloc")
+
+
+def muon_inject_copy_failure(plan: Plan, nth: int) -> None:
+    """The nth host-link copy of the plan's next offload step reports a failure
+    (MUON_ERR_CUDA) instead of being enqueued; -1 clears it."""
+    _check(_lib().muon_inject_copy_failure(plan.handle, int(nth)), "muon_inject_copy_failure")
 
 
 def muon_noalloc_scratch_bytes() -> int:

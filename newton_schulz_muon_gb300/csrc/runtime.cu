@@ -147,6 +147,12 @@ struct muon_plan_s {
   int64_t last_h2d_bytes = 0, last_d2h_bytes = 0;
   // per-iteration (a, b, c) set by muon_set_ns_schedule; empty: cfg's for every iteration
   std::vector<float> ns_sched;
+  // offload: recorded after the last writeback of each step, waited on by the next
+  // step's streams (a step that returned MUON_ERR_TIMEOUT may still be in flight)
+  cudaEvent_t offload_done = nullptr;
+  // host-link copy failure injection (muon_inject_copy_failure): the index, in the
+  // next offload step, of the copy reported as failed (-1: none)
+  int64_t fail_copy_at = -1;
   // process-unique id (never reused, unlike the plan's address)
   uint64_t id = 0;
   // the tile schedules as uploaded by the last bind (host copy kept for stream-ordered re-uploads)
@@ -973,6 +979,7 @@ muon_status bind_impl(muon_plan_t* p, void* dev_ptr, size_t bytes, cudaStream_t 
     }
     cudaEventCreate(&p->step_start);
     cudaEventCreate(&p->step_end);
+    cudaEventCreateWithFlags(&p->offload_done, cudaEventDisableTiming);
   }
   if (!stream_ordered) {
     e = cudaMemset(p->ws + p->off_status, 0, sizeof(DeviceStatus));
@@ -1092,6 +1099,8 @@ muon_status offload_zero_copy(muon_plan_t* p, const void* const* h_grads, void* 
   }
   int64_t h2d_bytes = 0, d2h_bytes = 0;
   cudaError_t e;
+  // after the previous step's kernels, even if that step returned before they finished
+  cudaStreamWaitEvent(cs, p->offload_done, 0);
   if (timing) cudaEventRecord(p->step_start, cs);
   for (size_t bi = 0; bi < p->buckets.size(); ++bi) {
     const Bucket& b = p->buckets[bi];
@@ -1132,7 +1141,7 @@ muon_status offload_zero_copy(muon_plan_t* p, const void* const* h_grads, void* 
     }
   }
   if (timing) cudaEventRecord(p->step_end, cs);
-  cudaEvent_t done = p->slot_d2h[0];  // the bind step creates at least one
+  cudaEvent_t done = p->offload_done;
   e = cudaEventRecord(done, cs);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   // drain: the host reads the results next
@@ -1181,10 +1190,25 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
   int64_t h2d_bytes = 0, d2h_bytes = 0;
   cudaError_t e;
   if (timing) cudaEventRecord(p->step_start, cs);
-  // the host buffers must not be touched by the previous step any more
+  // the host buffers must not be touched by the previous step any more: its
+  // compute (the stream's earlier work) and its writebacks, which are still in
+  // flight if it returned MUON_ERR_TIMEOUT or an error
   e = cudaEventRecord(p->slot_h2d[0], cs);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   cudaStreamWaitEvent(hs, p->slot_h2d[0], 0);
+  cudaStreamWaitEvent(hs, p->offload_done, 0);
+  cudaStreamWaitEvent(cs, p->offload_done, 0);
+  int64_t copy_index = 0;  // host-link copies enqueued so far (failure injection)
+  const int64_t fail_at = p->fail_copy_at;
+  p->fail_copy_at = -1;
+  auto injected = [&]() { return copy_index++ == fail_at; };
+  // a failure after some buckets' work was enqueued: later steps still wait for it
+  auto enqueue_fail = [&](cudaError_t err, const char* what) {
+    cudaEventRecord(p->offload_done, ds);
+    if (err == cudaSuccess)
+      return fail(MUON_ERR_CUDA, "%s: injected failure of host-link copy %lld", what, (long long)fail_at);
+    return cuda_fail(err, what);
+  };
   for (size_t bi = 0; bi < p->buckets.size(); ++bi) {
     const Bucket& b = p->buckets[bi];
     const int slot = (int)(bi % p->n_slots);
@@ -1203,11 +1227,13 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
         const int64_t me = t.rows * t.cols;
         const uint8_t* hg = static_cast<const uint8_t*>(h_grads[r.tensor]) + (size_t)r.first * t.stride * gs;
         const uint8_t* hm = static_cast<const uint8_t*>(h_momentum[r.tensor]) + (size_t)r.first * t.stride * 4;
+        if (injected()) return enqueue_fail(cudaSuccess, "host->device copy");
         e = cudaMemcpy2DAsync(sg + (size_t)eoff * gs, me * gs, hg, t.stride * gs, me * gs, r.count,
                               cudaMemcpyHostToDevice, hs);
+        if (e == cudaSuccess && injected()) return enqueue_fail(cudaSuccess, "host->device copy");
         if (e == cudaSuccess)
           e = cudaMemcpy2DAsync(sm + eoff, me * 4, hm, t.stride * 4, me * 4, r.count, cudaMemcpyHostToDevice, hs);
-        if (e != cudaSuccess) return cuda_fail(e, "host->device copy");
+        if (e != cudaSuccess) return enqueue_fail(e, "host->device copy");
         h2d_bytes += r.count * me * (int64_t)(gs + 4);
         run_off.emplace_back(&r, eoff);
         eoff += r.count * me;
@@ -1253,16 +1279,19 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
       const int64_t me = t.rows * t.cols;
       uint8_t* hm = static_cast<uint8_t*>(h_momentum[r.tensor]) + (size_t)r.first * t.stride * 4;
       uint8_t* hu = static_cast<uint8_t*>(h_update_out[r.tensor]) + (size_t)r.first * t.stride * 4;
+      if (injected()) return enqueue_fail(cudaSuccess, "device->host copy");
       e = cudaMemcpy2DAsync(hm, t.stride * 4, sm + off, me * 4, me * 4, r.count, cudaMemcpyDeviceToHost, ds);
+      if (e == cudaSuccess && injected()) return enqueue_fail(cudaSuccess, "device->host copy");
       if (e == cudaSuccess)
         e = cudaMemcpy2DAsync(hu, t.stride * 4, su + off, me * 4, me * 4, r.count, cudaMemcpyDeviceToHost, ds);
-      if (e != cudaSuccess) return cuda_fail(e, "device->host copy");
+      if (e != cudaSuccess) return enqueue_fail(e, "device->host copy");
       d2h_bytes += r.count * me * 8;
     }
     cudaEventRecord(p->slot_d2h[slot], ds);
     if (timing) cudaEventRecord(p->events[bi].d2h, ds);
   }
   if (timing) cudaEventRecord(p->step_end, ds);
+  cudaEventRecord(p->offload_done, ds);  // ds carries every bucket's writeback, in order
   // drain: the host reads the results next
   const auto t0 = std::chrono::steady_clock::now();
   for (int sidx = 0; sidx < p->n_slots && sidx < (int)p->buckets.size(); ++sidx) {
@@ -1278,6 +1307,13 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
   p->offload_last = true;
   p->last_h2d_bytes = h2d_bytes;
   p->last_d2h_bytes = d2h_bytes;
+  return MUON_OK;
+}
+
+muon_status muon_inject_copy_failure(muon_plan_t* p, int64_t nth) {
+  if (!p) return fail(MUON_ERR_INVALID, "plan is NULL");
+  if (nth < -1) return fail(MUON_ERR_INVALID, "nth must be >= -1");
+  p->fail_copy_at = nth;
   return MUON_OK;
 }
 
@@ -1368,6 +1404,7 @@ void muon_plan_destroy(muon_plan_t* p) {
         if (x) cudaEventDestroy(x);
     if (p->step_start) cudaEventDestroy(p->step_start);
     if (p->step_end) cudaEventDestroy(p->step_end);
+    if (p->offload_done) cudaEventDestroy(p->offload_done);
     cudaStreamDestroy(p->h2d_stream);
     cudaStreamDestroy(p->d2h_stream);
   }

@@ -327,6 +327,88 @@ def test_zero_copy_offload_is_bitwise_the_staged_one(m, shapes):
     assert m.muon_get_plan_info(p2).workspace_bytes < m.muon_get_plan_info(p1).workspace_bytes
 
 
+def _offload_check(wl, hM_prev, hM, hU):
+    """Every matrix of an offload step against the oracle, teacher forced from the
+    momentum the step started from."""
+    mu32, omu = oracle_constants(0.95, "ema")
+    coeffs = tuple(f32(v) for v in oracle.DEFAULT_COEFFS)
+    for i, (r, c, k) in enumerate(wl.shapes):
+        for j in range(k):
+            G = widen(wl.G[i][j], wl.g_dtype)
+            Mo = oracle.momentum_update(hM_prev[i][j], G, mu32, one_minus_mu=omu)
+            assert int(ulp_distance(hM[i][j], Mo).max()) <= 1, (i, j)
+            V = oracle.nesterov_blend(Mo, G, mu32, True, one_minus_mu=omu)
+            Uo = oracle.offload_update(oracle.newton_schulz(V, coeffs=coeffs, eps=f32(1e-7)), r, c)
+            assert rel_fro(hU[i][j], Uo) <= TOL_BF16, (i, j)
+
+
+def _offload_plan(m, wl, cap):
+    import torch
+    cfg = m.muon_config_default(offload=1, max_inflight=2)
+    cfg.grad_dtype = wl.g_dtype
+    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=cap, config=cfg)
+    m.allocate_workspace(plan)
+    hG = [_pinned(g, wl.g_dtype) for g in wl.G]
+    hM = [_pinned(x, synth.F32) for x in wl.M]
+    hU = [torch.empty(x.shape, dtype=torch.float32).pin_memory() for x in wl.M]
+    return plan, hG, hM, hU
+
+
+def test_offload_timeout_then_recovers(m):
+    # the failure path of the offload's bounded host wait, without a fault: a
+    # kernel holds the compute stream for 300 ms (the failure-path self-test's
+    # bounded wait on a barrier nothing arrives on), so the step cannot finish
+    # within its 50 ms and returns MUON_ERR_TIMEOUT.  Its work completes later and
+    # matches the oracle; the next step of the same plan matches it too.
+    import torch
+    wl = Workload([(256, 512, 3), (300, 200, 2), (128, 640, 4)], m_sigma=0.02, g_sigma=1e-3)
+    plan, hG, hM, hU = _offload_plan(m, wl, cap=600_000)
+    assert m.muon_get_plan_info(plan).n_buckets >= 3
+    cs = torch.cuda.Stream()
+    M0 = [x.numpy().copy() for x in hM]
+    m.muon_selftest_wait_timeout(plan, 300_000, stream=cs)
+    with pytest.raises(m.MuonError) as e:
+        m.muon_offload_step(plan, hG, hM, hU, 0.95, True, 5, compute=cs, timeout_ms=50)
+    assert e.value.status == m.MUON_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    with pytest.raises(m.MuonError) as e:            # the self-test's own record
+        m.muon_sync(plan, stream=cs)
+    assert e.value.status == m.MUON_ERR_DEVICE
+    M1 = [x.numpy().copy() for x in hM]
+    _offload_check(wl, M0, M1, [u.numpy() for u in hU])
+    m.muon_offload_step(plan, hG, hM, hU, 0.95, True, 5, compute=cs, timeout_ms=120_000)
+    _offload_check(wl, M1, [x.numpy() for x in hM], [u.numpy() for u in hU])
+    assert m.muon_sync(plan, stream=cs) == (m.MUON_OK, 0)
+
+
+@pytest.mark.parametrize("nth", [0, 3, 6])
+def test_offload_injected_copy_failure_then_recovers(m, nth):
+    # a host-link copy that fails to enqueue (injected: the call reports it as if
+    # cudaMemcpy2DAsync had failed).  Copies per bucket: an upload of G and of M
+    # per run, then a writeback of M and of U' per run; the first bucket holds one
+    # run (copies 0-3), the second two (4-11).  nth 0: the first upload, nothing
+    # enqueued; 3: the first bucket's U' writeback, after its M writeback; 6: the
+    # second bucket's second run, after the whole first bucket.  The step returns
+    # MUON_ERR_CUDA, the work enqueued before the failure completes, and the next
+    # step of the same plan runs to the end and matches the oracle from whatever
+    # momentum the failed step left in each matrix.
+    import torch
+    wl = Workload([(256, 512, 3), (300, 200, 2), (128, 640, 4)], m_sigma=0.02, g_sigma=1e-3)
+    plan, hG, hM, hU = _offload_plan(m, wl, cap=600_000)
+    assert m.muon_get_plan_info(plan).n_buckets >= 3
+    M0 = [x.numpy().copy() for x in hM]
+    m.muon_inject_copy_failure(plan, nth)
+    with pytest.raises(m.MuonError) as e:
+        m.muon_offload_step(plan, hG, hM, hU, 0.95, True, 5)
+    assert e.value.status == m.MUON_ERR_CUDA and "injected" in str(e.value)
+    torch.cuda.synchronize()
+    M1 = [x.numpy().copy() for x in hM]
+    changed = sum(int(not np.array_equal(a, b)) for a, b in zip(M0, M1))
+    assert changed == {0: 0, 3: 1, 6: 1}[nth]      # tensors whose momentum the failed step wrote back
+    m.muon_offload_step(plan, hG, hM, hU, 0.95, True, 5)   # the injection was cleared
+    _offload_check(wl, M1, [x.numpy() for x in hM], [u.numpy() for u in hU])
+
+
 def test_offload_rejects_pageable_host_memory(m):
     import torch
     wl = Workload([(64, 128)])
