@@ -333,6 +333,35 @@ typedef struct {
 } muon_stats;
 muon_status muon_get_stats(const muon_plan_t* plan, muon_stats* out);
 
+/* Defines: "Muon Optimizer + FSDP", section 需要记录的指标 (metrics to log per
+ * Muon bucket: its logical shape, tensor count, full bytes, estimated
+ * Newton-Schulz workspace bytes, newton_schulz_time_ms and the transfer times and
+ * bytes around it).
+ * Bucket b: its shape and sizes (pure host), the host-link bytes it moved in the
+ * last offload step (0 after muon_step), and, with cfg.timing = 1, the times of
+ * its phases in the last step in ms (waits for that step's events).  prep_ms is 0
+ * when the small-matrix kernel computed the momentum (it is then part of ns_ms). */
+typedef struct {
+  int64_t n_matrices, n_groups;
+  int64_t m, n;                  /* wide form of its first group */
+  int64_t bytes;                 /* wide-form bf16 bytes of its matrices */
+  int64_t ns_workspace_bytes;    /* its Newton-Schulz region in the workspace */
+  double prep_ms, ns_ms, apply_ms, h2d_ms, d2h_ms;
+  int64_t h2d_bytes, d2h_bytes;
+} muon_bucket_stats;
+muon_status muon_get_bucket_stats(const muon_plan_t* plan, int64_t b, muon_bucket_stats* out);
+
+/* Defines: "Muon Optimizer + FSDP", section 需要记录的指标 (what to log to tell
+ * where the step's numbers come from); the quantity is the Frobenius norm the
+ * Newton-Schulz normalisation divides by.
+ * Copies ||V||_F of every matrix's Newton-Schulz input in the plan's last step
+ * (V the Nesterov look-ahead or the new momentum, before the bf16 cast) into
+ * out[n], n = the plan's matrix count, in tensor order (shapes[0]'s `count`
+ * matrices first).  A non-finite norm is reported as it came out (inf or NaN).
+ * Waits for `stream`.  Errors: MUON_ERR_INVALID, MUON_ERR_NO_WORKSPACE,
+ * MUON_ERR_CUDA. */
+muon_status muon_get_input_norms(const muon_plan_t* plan, float* out, int64_t n, void* stream);
+
 /* Text of the last error reported by an entry point on the calling thread
  * (empty string if none).  Valid until that thread's next call. */
 const char* muon_last_error(void);

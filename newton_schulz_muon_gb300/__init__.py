@@ -62,6 +62,13 @@ class muon_bucket_info(ctypes.Structure):
                 ("momentum_in_ns_kernel", c_int64)]
 
 
+class muon_bucket_stats(ctypes.Structure):
+    _fields_ = [("n_matrices", c_int64), ("n_groups", c_int64), ("m", c_int64), ("n", c_int64),
+                ("bytes", c_int64), ("ns_workspace_bytes", c_int64), ("prep_ms", ctypes.c_double),
+                ("ns_ms", ctypes.c_double), ("apply_ms", ctypes.c_double), ("h2d_ms", ctypes.c_double),
+                ("d2h_ms", ctypes.c_double), ("h2d_bytes", c_int64), ("d2h_bytes", c_int64)]
+
+
 class muon_stats(ctypes.Structure):
     _fields_ = [("prep_ms", ctypes.c_double), ("ns_ms", ctypes.c_double), ("apply_ms", ctypes.c_double),
                 ("h2d_ms", ctypes.c_double), ("d2h_ms", ctypes.c_double), ("step_ms", ctypes.c_double),
@@ -99,6 +106,8 @@ def _load() -> ctypes.CDLL:
                                         c_int32, c_float, c_int32, P]),
         "muon_noalloc_scratch_bytes": (c_size_t, []),
         "muon_inject_copy_failure": (c_int32, [P, c_int64]),
+        "muon_get_bucket_stats": (c_int32, [P, c_int64, POINTER(muon_bucket_stats)]),
+        "muon_get_input_norms": (c_int32, [P, POINTER(c_float), c_int64, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -297,6 +306,20 @@ def muon_get_stats(plan: Plan) -> muon_stats:
     st = muon_stats()
     _check(_lib().muon_get_stats(plan.handle, byref(st)), "muon_get_stats")
     return st
+
+
+def muon_get_bucket_stats(plan: Plan, b: int) -> muon_bucket_stats:
+    st = muon_bucket_stats()
+    _check(_lib().muon_get_bucket_stats(plan.handle, int(b), byref(st)), "muon_get_bucket_stats")
+    return st
+
+
+def muon_get_input_norms(plan: Plan, stream=None):
+    """||V||_F of every matrix's Newton-Schulz input in the last step, tensor order."""
+    n = int(muon_get_plan_info(plan).n_matrices)
+    out = (c_float * n)()
+    _check(_lib().muon_get_input_norms(plan.handle, out, n, _stream_ptr(stream)), "muon_get_input_norms")
+    return list(out)
 
 
 def muon_status_string(status: int) -> str:

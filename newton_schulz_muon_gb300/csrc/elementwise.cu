@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const __grid_constan
     const bool finite = isfinite(tot);
     a.scale[mat] = finite ? (float)(1.0 / (sqrt(tot) + (double)a.eps)) : 0.f;
     a.flags[mat] = finite ? 0 : 1;
+    s.norm_out[mat - s.mat0] = (float)sqrt(tot);
     if (!finite) atomicAdd(&a.status->nonfinite, 1u);
   }
 }

@@ -44,6 +44,7 @@ struct PrepSeg {
   int32_t tiles_per_mat; // tiles per matrix
   int32_t mat0;          // bucket-local index of the run's first matrix
   int32_t pad_;
+  float* norm_out;       // ||V||_F of the run's first matrix in the plan's norm record
 };
 
 struct PrepArgs {
@@ -163,6 +164,7 @@ struct SmallPrepSeg {
   int64_t stride;        // elements between consecutive matrices in g and m
   int32_t mat0;          // bucket-local index of the run's first matrix
   int32_t pad_;
+  float* norm_out;       // ||V||_F of the run's first matrix in the plan's norm record
 };
 
 struct SmallArgs {

@@ -456,6 +456,8 @@ __device__ __forceinline__ float prep_scale(const SmallArgs& a, int mat, const f
   if (threadIdx.x == 64) {
     a.scale[mat] = s;
     a.flags[mat] = finite ? 0 : 1;
+    const SmallPrepSeg& P = prep_seg(a, mat);
+    P.norm_out[mat - P.mat0] = (float)sqrt(tot);
     if (!finite) atomicAdd(&a.status->nonfinite, 1u);
   }
   return s;

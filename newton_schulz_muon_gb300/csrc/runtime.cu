@@ -34,6 +34,8 @@
 #include <tuple>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kernels.h"
 #include "muon.h"
 
@@ -57,6 +59,23 @@ muon_status fail(muon_status s, const char* fmt, ...) {
 muon_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MUON_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+// NVTX range around the host-side enqueue of a step and of each of its buckets,
+// so that a profiler's timeline names them ("Muon Optimizer + FSDP", section
+// 需要记录的指标: per-bucket records).  A no-op unless a tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* fmt, ...) __attribute__((format(printf, 2, 3))) {
+    char buf[96];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    nvtxRangePushA(buf);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr size_t kAlign = 1024;
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -130,6 +149,8 @@ struct muon_plan_s {
   int64_t n_matrices = 0;
   // layout
   size_t off_status = 0, off_scale = 0, off_flags = 0, off_partials = 0, off_ns = 0, off_stage = 0;
+  size_t off_norms = 0;               // ||V||_F of every matrix (tensor order) in the last step
+  std::vector<int64_t> tensor_first;  // index of each tensor's first matrix in that order
   size_t off_sched = 0, sched_bytes = 0;
   size_t ns_bytes = 0, slot_bytes = 0, ws_bytes = 0;
   int n_slots = 0;
@@ -145,6 +166,7 @@ struct muon_plan_s {
   cudaEvent_t step_start = nullptr, step_end = nullptr;
   bool offload_last = false;
   int64_t last_h2d_bytes = 0, last_d2h_bytes = 0;
+  std::vector<int64_t> bucket_h2d_bytes, bucket_d2h_bytes;  // per bucket, last offload step
   // per-iteration (a, b, c) set by muon_set_ns_schedule; empty: cfg's for every iteration
   std::vector<float> ns_sched;
   // offload: recorded after the last writeback of each step, waited on by the next
@@ -403,6 +425,12 @@ muon_status build_plan(muon_plan_t* p, const muon_shape* shapes, int32_t n, cons
   p->off_scale = off; off = align_up(off + (size_t)p->max_mats * 4, kAlign);
   p->off_flags = off; off = align_up(off + (size_t)p->max_mats * 4, kAlign);
   p->off_partials = off; off = align_up(off + (size_t)p->max_tiles * 4, kAlign);
+  p->off_norms = off; off = align_up(off + (size_t)p->n_matrices * 4, kAlign);
+  p->tensor_first.assign(p->tensors.size(), 0);
+  for (size_t i = 1; i < p->tensors.size(); ++i)
+    p->tensor_first[i] = p->tensor_first[i - 1] + p->tensors[i - 1].count;
+  p->bucket_h2d_bytes.assign(p->buckets.size(), 0);
+  p->bucket_d2h_bytes.assign(p->buckets.size(), 0);
   p->off_ns = off; off = align_up(off + ns_max, kAlign);
   p->ns_bytes = ns_max;
   // tile schedules, one per bucket and GEMM phase: offsets (clusters + 1) and tiles
@@ -476,6 +504,7 @@ void make_prep_args(const muon_plan_t* p, const Bucket& b, F ptr, float mu, int 
       s.tiles_c = (int32_t)cdiv(t.cols, kPrepTile);
       s.tiles_per_mat = (int32_t)tiles_of(t.rows, t.cols);
       s.mat0 = (int32_t)mat;
+      s.norm_out = at<float>(p, p->off_norms) + p->tensor_first[r.tensor] + r.first;
       tile += r.count * s.tiles_per_mat;
       mat += r.count;
     }
@@ -634,6 +663,7 @@ muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cuda
       sa.pseg[i].m = prep->seg[i].m;
       sa.pseg[i].stride = prep->seg[i].stride;
       sa.pseg[i].mat0 = prep->seg[i].mat0;
+      sa.pseg[i].norm_out = prep->seg[i].norm_out;
     }
   }
   cudaError_t e = launch_ns_small(sa, p->num_sms, st);
@@ -1023,9 +1053,14 @@ muon_status muon_step(muon_plan_t* p, void* const* params, const void* const* gr
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool timing = p->cfg.timing != 0;
   const size_t gs = grad_size(p->cfg), ps = param_size(p->cfg);
+  std::fill(p->bucket_h2d_bytes.begin(), p->bucket_h2d_bytes.end(), 0);
+  std::fill(p->bucket_d2h_bytes.begin(), p->bucket_d2h_bytes.end(), 0);
+  NvtxRange step_range("muon_step: %zu buckets", p->buckets.size());
   if (timing) cudaEventRecord(p->step_start, st);
   for (size_t bi = 0; bi < p->buckets.size(); ++bi) {
     const Bucket& b = p->buckets[bi];
+    NvtxRange bucket_range("muon bucket %zu: %lld matrices, %lld x %lld", bi, (long long)b.n_mats,
+                           (long long)b.groups[0].m, (long long)b.groups[0].n);
     auto ptrs = [&](const Run& r) {
       const TensorInfo& t = p->tensors[r.tensor];
       RunPtrs rp;
@@ -1098,6 +1133,8 @@ muon_status offload_zero_copy(muon_plan_t* p, const void* const* h_grads, void* 
     if ((s = mapped(h_update_out[i], "h_update_out", i, &du[i])) != MUON_OK) return s;
   }
   int64_t h2d_bytes = 0, d2h_bytes = 0;
+  std::fill(p->bucket_h2d_bytes.begin(), p->bucket_h2d_bytes.end(), 0);
+  std::fill(p->bucket_d2h_bytes.begin(), p->bucket_d2h_bytes.end(), 0);
   cudaError_t e;
   // after the previous step's kernels, even if that step returned before they finished
   cudaStreamWaitEvent(cs, p->offload_done, 0);
@@ -1118,6 +1155,8 @@ muon_status offload_zero_copy(muon_plan_t* p, const void* const* h_grads, void* 
         const TensorInfo& t = p->tensors[r.tensor];
         h2d_bytes += r.count * t.rows * t.cols * (int64_t)(gs + 4);
         d2h_bytes += r.count * t.rows * t.cols * 8;
+        p->bucket_h2d_bytes[bi] += r.count * t.rows * t.cols * (int64_t)(gs + 4);
+        p->bucket_d2h_bytes[bi] += r.count * t.rows * t.cols * 8;
       }
     if (timing) {
       cudaEventRecord(p->events[bi].start, cs);
@@ -1188,6 +1227,8 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
   const size_t gs = grad_size(p->cfg);
   const bool timing = p->cfg.timing != 0;
   int64_t h2d_bytes = 0, d2h_bytes = 0;
+  std::fill(p->bucket_h2d_bytes.begin(), p->bucket_h2d_bytes.end(), 0);
+  std::fill(p->bucket_d2h_bytes.begin(), p->bucket_d2h_bytes.end(), 0);
   cudaError_t e;
   if (timing) cudaEventRecord(p->step_start, cs);
   // the host buffers must not be touched by the previous step any more: its
@@ -1209,8 +1250,11 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
       return fail(MUON_ERR_CUDA, "%s: injected failure of host-link copy %lld", what, (long long)fail_at);
     return cuda_fail(err, what);
   };
+  NvtxRange step_range("muon_offload_step: %zu buckets", p->buckets.size());
   for (size_t bi = 0; bi < p->buckets.size(); ++bi) {
     const Bucket& b = p->buckets[bi];
+    NvtxRange bucket_range("muon offload bucket %zu: %lld matrices, %lld x %lld", bi, (long long)b.n_mats,
+                           (long long)b.groups[0].m, (long long)b.groups[0].n);
     const int slot = (int)(bi % p->n_slots);
     uint8_t* sbase = p->ws + p->off_stage + (size_t)slot * p->slot_bytes;
     uint8_t* sg = sbase;
@@ -1235,6 +1279,7 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
           e = cudaMemcpy2DAsync(sm + eoff, me * 4, hm, t.stride * 4, me * 4, r.count, cudaMemcpyHostToDevice, hs);
         if (e != cudaSuccess) return enqueue_fail(e, "host->device copy");
         h2d_bytes += r.count * me * (int64_t)(gs + 4);
+        p->bucket_h2d_bytes[bi] += r.count * me * (int64_t)(gs + 4);
         run_off.emplace_back(&r, eoff);
         eoff += r.count * me;
       }
@@ -1286,6 +1331,7 @@ muon_status muon_offload_step(muon_plan_t* p, const void* const* h_grads, void* 
         e = cudaMemcpy2DAsync(hu, t.stride * 4, su + off, me * 4, me * 4, r.count, cudaMemcpyDeviceToHost, ds);
       if (e != cudaSuccess) return enqueue_fail(e, "device->host copy");
       d2h_bytes += r.count * me * 8;
+      p->bucket_d2h_bytes[bi] += r.count * me * 8;
     }
     cudaEventRecord(p->slot_d2h[slot], ds);
     if (timing) cudaEventRecord(p->events[bi].d2h, ds);
@@ -1373,6 +1419,49 @@ muon_status muon_get_stats(const muon_plan_t* p, muon_stats* out) {
   out->h2d_bytes = p->last_h2d_bytes;
   out->d2h_bytes = p->last_d2h_bytes;
   out->n_buckets = (int64_t)p->buckets.size();
+  return MUON_OK;
+}
+
+muon_status muon_get_bucket_stats(const muon_plan_t* p, int64_t b, muon_bucket_stats* out) {
+  if (!p || !out) return fail(MUON_ERR_INVALID, "NULL argument");
+  if (b < 0 || b >= (int64_t)p->buckets.size()) return fail(MUON_ERR_INVALID, "bucket index out of range");
+  std::memset(out, 0, sizeof(*out));
+  const Bucket& k = p->buckets[b];
+  out->n_matrices = k.n_mats;
+  out->n_groups = (int64_t)k.groups.size();
+  out->m = k.groups[0].m;
+  out->n = k.groups[0].n;
+  out->bytes = k.bytes;
+  out->ns_workspace_bytes = (int64_t)k.ns_bytes;
+  out->h2d_bytes = p->bucket_h2d_bytes[b];
+  out->d2h_bytes = p->bucket_d2h_bytes[b];
+  if (!p->cfg.timing) return MUON_OK;
+  if (!p->step_end) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
+  cudaError_t e = cudaEventSynchronize(p->step_end);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+  const BucketEvents& ev = p->events[b];
+  if (p->offload_last) {
+    out->h2d_ms = elapsed(ev.start, ev.h2d);
+    out->ns_ms = elapsed(ev.prep, ev.ns);
+    out->apply_ms = elapsed(ev.ns, ev.apply);
+    out->d2h_ms = elapsed(ev.d2h_start, ev.d2h);
+  } else {
+    out->prep_ms = elapsed(ev.start, ev.prep);
+    out->ns_ms = elapsed(ev.prep, ev.ns);
+    out->apply_ms = elapsed(ev.ns, ev.apply);
+  }
+  return MUON_OK;
+}
+
+muon_status muon_get_input_norms(const muon_plan_t* p, float* out, int64_t n, void* stream) {
+  if (!p || !out) return fail(MUON_ERR_INVALID, "NULL argument");
+  if (n != p->n_matrices) return fail(MUON_ERR_INVALID, "n %lld != %lld matrices in the plan", (long long)n,
+                                      (long long)p->n_matrices);
+  if (!p->ws) return fail(MUON_ERR_NO_WORKSPACE, "no workspace bound");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(out, p->ws + p->off_norms, (size_t)n * sizeof(float), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "norm read");
   return MUON_OK;
 }
 

@@ -452,3 +452,63 @@ def test_resume_from_copied_state_is_bitwise_identical(m):
     torch.cuda.synchronize()
     for a, b in zip(run.dW + run.dM, res.dW + res.dM):
         assert torch.equal(a, b)
+
+
+# --- metrics: per-bucket records and input norms ("Muon Optimizer + FSDP", 需要记录的指标) ---
+
+@pytest.mark.parametrize("g_dtype", [synth.BF16, synth.F32])
+def test_input_norms_match_the_oracle(m, g_dtype):
+    # ||V||_F of every matrix, tensor order: grouped-GEMM buckets, small-matrix
+    # buckets (bf16 gradients: the norm is summed inside the small kernel; fp32:
+    # by the momentum kernel), a tall matrix; a NaN matrix reports a non-finite norm
+    import math
+    wl = Workload([(256, 512), (128, 640, 3), (700, 96), (64, 128, 2)], m_sigma=0.02, g_sigma=1e-3,
+                  g_dtype=g_dtype)
+    g = wl.dG[3].clone()
+    g[1, 2, 3] = float("nan")
+    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=300_000)
+    assert m.muon_get_plan_info(plan).n_buckets >= 3
+    m.allocate_workspace(plan)
+    m.muon_step(plan, wl.dW, wl.dG[:3] + [g], wl.dM, 0.02, 0.95, True, 0.0, 5)
+    st, nf = m.muon_sync(plan)
+    assert st == m.MUON_WARN_NONFINITE and nf == 1
+    norms = m.muon_get_input_norms(plan)
+    mu32, omu = oracle_constants(0.95, "ema")
+    idx = 0
+    for i, (r, c, k) in enumerate(wl.shapes):
+        for j in range(k):
+            if (i, j) == (3, 1):
+                assert not math.isfinite(norms[idx])
+            else:
+                G = widen(wl.G[i][j], g_dtype)
+                Mo = oracle.momentum_update(wl.M[i][j], G, mu32, one_minus_mu=omu)
+                V = oracle.nesterov_blend(Mo, G, mu32, True, one_minus_mu=omu)
+                assert abs(norms[idx] - np.linalg.norm(V)) <= 1e-5 * np.linalg.norm(V), (i, j)
+            idx += 1
+
+
+def test_bucket_stats_add_up_to_the_step(m):
+    import torch
+    wl = Workload([(256, 512, 2), (128, 640, 3), (300, 200)], m_sigma=0.02, g_sigma=1e-3)
+    cfg = m.muon_config_default(timing=1)
+    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=300_000, config=cfg)
+    m.allocate_workspace(plan)
+    m.muon_step(plan, wl.dW, wl.dG, wl.dM, 0.02, 0.95, True, 0.0, 5)
+    torch.cuda.synchronize()
+    total = m.muon_get_stats(plan)
+    info = m.muon_get_plan_info(plan)
+    bs = [m.muon_get_bucket_stats(plan, b) for b in range(info.n_buckets)]
+    assert sum(b.n_matrices for b in bs) == info.n_matrices == 6
+    assert sum(b.ns_ms for b in bs) == pytest.approx(total.ns_ms, rel=1e-6)
+    assert sum(b.prep_ms for b in bs) == pytest.approx(total.prep_ms, rel=1e-6, abs=1e-9)
+    assert all(b.ns_ms > 0 and b.h2d_bytes == 0 and b.ns_workspace_bytes > 0 for b in bs)
+    for b, want in zip(bs, (m.muon_get_bucket_info(plan, i) for i in range(info.n_buckets))):
+        assert (b.m, b.n, b.bytes, b.n_groups) == (want.m, want.n, want.bytes, want.n_groups)
+    # offload: per-bucket host-link bytes add up to the step's
+    wl = Workload([(256, 512, 3), (300, 200, 2)], m_sigma=0.02, g_sigma=1e-3)
+    _, _, st, plan = _offload(m, wl, cap=600_000, inflight=2)
+    info = m.muon_get_plan_info(plan)
+    bs = [m.muon_get_bucket_stats(plan, b) for b in range(info.n_buckets)]
+    assert sum(b.h2d_bytes for b in bs) == st.h2d_bytes == sum(r * c * k * 6 for r, c, k in wl.shapes)
+    assert sum(b.d2h_bytes for b in bs) == st.d2h_bytes
+    assert all(b.h2d_ms > 0 and b.d2h_ms > 0 for b in bs)
