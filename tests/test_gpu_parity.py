@@ -466,7 +466,8 @@ def test_input_norms_match_the_oracle(m, g_dtype):
                   g_dtype=g_dtype)
     g = wl.dG[3].clone()
     g[1, 2, 3] = float("nan")
-    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=300_000)
+    plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=300_000,
+                       config=m.muon_config_default(grad_dtype=g_dtype))
     assert m.muon_get_plan_info(plan).n_buckets >= 3
     m.allocate_workspace(plan)
     m.muon_step(plan, wl.dW, wl.dG[:3] + [g], wl.dM, 0.02, 0.95, True, 0.0, 5)
