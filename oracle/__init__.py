@@ -154,6 +154,45 @@ def newton_schulz(V, steps: int = DEFAULT_NS_STEPS, coeffs=DEFAULT_COEFFS,
 
 
 # ---------------------------------------------------------------------------
+# the "gram" Newton-Schulz method (DeepSpeed PR "[Muon] CPU offload: pin the
+# momentum and overlap the host writeback", section Tests: per-head shard tests
+# parametrised over "gram" and "standard"; DeepSpeed issue "[RFC] ... ZeRO CPU
+# Offload", follow-up list: the gram method gives results that differ from the
+# quintic iteration's in floating point)
+# ---------------------------------------------------------------------------
+# The pages name the method and say only that its results differ in floating
+# point.  The reading taken here is the iteration rewritten on the Gram matrix:
+# with X_{k+1} = Q_k X_k and Q_k = a I + b A_k + c A_k^2, A_k = X_k X_k^T, one has
+# A_{k+1} = Q_k A_k Q_k (Q_k is symmetric) and X_K = (Q_{K-1} ... Q_0) X_0, so the
+# whole iteration runs on m x m matrices between one product X_0 X_0^T and one
+# final product R X_0.  In exact arithmetic it is the quintic iteration itself.
+# A restart at iteration r forms X_r = R_r X_0 and A_r = X_r X_r^T afresh.
+
+def newton_schulz_gram(V, steps: int = DEFAULT_NS_STEPS, coeffs=DEFAULT_COEFFS,
+                       eps: float = DEFAULT_EPS, restarts=()) -> np.ndarray:
+    """The Gram-form Newton-Schulz iteration of the whole 2-D matrix V (fp64).
+
+    Orient wide, normalise by the Frobenius norm, A = X X^T, R = I; per iteration
+    (a restart first when k is in ``restarts``: X = R X, A = X X^T, R = I)
+    Q = a I + b A + c A A, A = Q A Q, R = Q R; finally U = R X, un-oriented."""
+    X, transposed = orient(V)
+    X = frobenius_normalize(X, eps)
+    m = X.shape[0]
+    A = X @ X.T
+    R = np.eye(m)
+    for k, (a, b, c) in enumerate(coefficient_schedule(coeffs, steps)):
+        if k in restarts:
+            X = R @ X
+            A = X @ X.T
+            R = np.eye(m)
+        Q = a * np.eye(m) + b * A + c * (A @ A)
+        A = Q @ A @ Q
+        R = Q @ R
+    U = R @ X
+    return U.T if transposed else U
+
+
+# ---------------------------------------------------------------------------
 # per-iteration coefficients (DeepSpeed issue "[RFC] Enable Correct and
 # High-Performance Muon Optimizer under ZeRO CPU Offload", follow-up list:
 # Newton-Schulz with per-iteration optimised coefficients, "Polar Express",
@@ -270,15 +309,21 @@ def offload_update(U, rows: int, cols: int) -> np.ndarray:
 def muon_matrix_step(W, M, G, lr: float, mu: float, nesterov: bool = True, wd: float = 0.0,
                      ns_steps: int = DEFAULT_NS_STEPS, coeffs: Sequence[float] = DEFAULT_COEFFS,
                      eps: float = DEFAULT_EPS, form: str = "ema",
-                     one_minus_mu: float | None = None):
+                     one_minus_mu: float | None = None, method: str = "standard"):
     """One Muon step of one logical matrix.
 
     Returns (W_new fp64, M_new fp32, U fp64).  The caller rounds W_new to the
-    storage dtype of its weights.
+    storage dtype of its weights.  ``method``: "standard" (the quintic iteration on
+    X) or "gram" (the same iteration on the Gram matrix, newton_schulz_gram).
     """
     M_new = momentum_update(M, G, mu, form, one_minus_mu)
     V = nesterov_blend(M_new, G, mu, nesterov, form, one_minus_mu)
-    U = newton_schulz(V, ns_steps, coeffs, eps)
+    if method == "gram":
+        U = newton_schulz_gram(V, ns_steps, coeffs, eps)
+    elif method == "standard":
+        U = newton_schulz(V, ns_steps, coeffs, eps)
+    else:
+        raise ValueError(f"unknown Newton-Schulz method {method!r}")
     W_new = apply_update(W, U, lr, wd)
     return W_new, M_new, U
 

@@ -291,3 +291,76 @@ def test_muon_step_over_tensors_matches_per_matrix():
                                             G[sl].reshape(rows, cols), 0.02, 0.95)
         assert np.array_equal(Wn[sl], w1.reshape(-1))
         assert np.array_equal(Mn[sl], m1.reshape(-1))
+
+
+# --- the "gram" Newton-Schulz method ------------------------------------------
+
+@pytest.mark.parametrize("shape", [(3, 5), (8, 8), (17, 4), (64, 128), (1, 7), (9, 1), (40, 24)])
+@pytest.mark.parametrize("steps", [0, 1, 5])
+def test_gram_method_svd_closed_form(shape, steps):
+    # the Gram-form iteration is the quintic iteration rewritten on X X^T: its
+    # result is P p^steps(s / (||s|| + eps)) Q^T like the standard form's
+    V = _rand(shape, 90 + steps)
+    assert _rel(oracle.newton_schulz_gram(V, steps), _closed_form(V, steps)) < 1e-10
+
+
+@pytest.mark.parametrize("restarts", [(), (2,), (1, 3), (0, 4)])
+def test_gram_method_restarts_change_nothing_in_exact_arithmetic(restarts):
+    V = _rand((24, 70), 91)
+    assert _rel(oracle.newton_schulz_gram(V, 5, restarts=restarts), oracle.newton_schulz(V, 5)) < 1e-10
+
+
+def test_gram_method_with_a_schedule_and_transpose():
+    co = [(3.0, -3.2, 1.2), (2.5, -2.0, 0.6), (15 / 8, -10 / 8, 3 / 8)]
+    V = _rand((50, 20), 92)                       # tall: transposed and back
+    assert _rel(oracle.newton_schulz_gram(V, 4, co), oracle.newton_schulz(V, 4, co)) < 1e-10
+    assert _rel(oracle.newton_schulz_gram(V.T, 4, co), oracle.newton_schulz_gram(V, 4, co).T) < 1e-13
+
+
+def test_gram_method_brute_force_one_iteration():
+    # one iteration written out with explicit loops on a 2 x 3 matrix:
+    # A = X X^T, Q = a I + b A + c A A, U = Q X
+    V = np.array([[1.0, -2.0, 0.5], [0.25, 3.0, -1.0]])
+    fro = math.sqrt(sum(v * v for v in V.ravel()))
+    X = V / (fro + EPS)
+    A = [[sum(X[i][k] * X[j][k] for k in range(3)) for j in range(2)] for i in range(2)]
+    AA = [[sum(A[i][k] * A[k][j] for k in range(2)) for j in range(2)] for i in range(2)]
+    Q = [[A_ * (i == j) + B_ * A[i][j] + C_ * AA[i][j] for j in range(2)] for i in range(2)]
+    U = np.array([[sum(Q[i][k] * X[k][j] for k in range(2)) for j in range(3)] for i in range(2)])
+    assert _rel(oracle.newton_schulz_gram(V, 1), U) < 1e-14
+
+
+def test_gram_method_differs_from_the_standard_form_only_by_rounding():
+    # in float32 the two forms round different operations, so they do not agree
+    # bit for bit; in float64 they agree to 1e-10 (the pins above)
+    V = _rand((32, 256), 93)
+
+    def f32_standard(V):
+        X = (V / np.linalg.norm(V)).astype(np.float32)
+        for _ in range(5):
+            A = X @ X.T
+            X = np.float32(A_) * X + (np.float32(B_) * A + np.float32(C_) * (A @ A)) @ X
+        return X
+
+    def f32_gram(V):
+        X = (V / np.linalg.norm(V)).astype(np.float32)
+        A, R, I = X @ X.T, np.eye(32, dtype=np.float32), np.eye(32, dtype=np.float32)
+        for _ in range(5):
+            Q = np.float32(A_) * I + np.float32(B_) * A + np.float32(C_) * (A @ A)
+            A, R = Q @ A @ Q, Q @ R
+        return R @ X
+
+    s, g = f32_standard(V), f32_gram(V)
+    assert 0 < _rel(g, s) < 1e-4
+    assert _rel(g, oracle.newton_schulz(V)) < 1e-4 and _rel(s, oracle.newton_schulz(V)) < 1e-4
+
+
+def test_full_step_gram_method():
+    W = 0.02 * _rand((6, 9), 94)
+    M = (0.02 * _rand((6, 9), 95)).astype(np.float32)
+    G = _rand((6, 9), 96).astype(np.float32)
+    Ws, Ms, Us = oracle.muon_matrix_step(W, M, G, 0.02, 0.95, True, 0.01)
+    Wg, Mg, Ug = oracle.muon_matrix_step(W, M, G, 0.02, 0.95, True, 0.01, method="gram")
+    assert np.array_equal(Ms, Mg) and _rel(Ug, Us) < 1e-10 and _rel(Wg, Ws) < 1e-12
+    with pytest.raises(ValueError):
+        oracle.muon_matrix_step(W, M, G, 0.02, 0.95, method="cubic")
