@@ -69,6 +69,20 @@ typedef int32_t muon_status;
                                  other buckets run three grouped GEMM launches per iteration */
 #define MUON_NS_KERNEL_GEMM 1 /* always the grouped GEMM launches */
 
+/* Newton-Schulz method (DeepSpeed PR "[Muon] CPU offload: pin the momentum and
+ * overlap the host writeback", section Tests, names a "gram" and a "standard"
+ * method; the pages give no more):
+ *   STANDARD  X_{k+1} = a X_k + (b A_k + c A_k A_k) X_k with A_k = X_k X_k^T;
+ *   GRAM      the same iteration rewritten on the Gram matrix: A_{k+1} = Q_k A_k Q_k,
+ *             Q_k = a I + b A_k + c A_k A_k, and U = (Q_{K-1} ... Q_0) X_0, so X is
+ *             read twice whatever the iteration count.  Equal in exact arithmetic;
+ *             in this library the m x m products are split into bf16 high and low
+ *             parts (about 16 bits per operand), so GRAM is also the more accurate.
+ *             Only buckets run by the small-matrix kernel (every matrix with
+ *             min(rows, cols) <= 128, bf16 arithmetic, ns_kernel AUTO). */
+#define MUON_NS_METHOD_STANDARD 0
+#define MUON_NS_METHOD_GRAM 1
+
 /* Newton-Schulz iterations per step: ns_steps in [0, MUON_MAX_NS_STEPS] */
 #define MUON_MAX_NS_STEPS 16
 
@@ -112,12 +126,14 @@ typedef struct {
                                 matrices, n and matrix strides multiples of 8) compute their
                                 momentum, norm and X0 in that kernel's first pass; 0: the
                                 momentum kernel runs first */
-  int32_t reserved[1];
+  int32_t ns_method;         /* MUON_NS_METHOD_STANDARD or MUON_NS_METHOD_GRAM */
+  int32_t reserved[2];
 } muon_config;
 
 /* Fills *cfg with (3.4445, -4.7750, 2.0315), eps 1e-7, bf16 NS, EMA momentum,
  * bf16 gradients, fp32 weights, max_inflight 1, skip_nonfinite 1, timing 0,
- * offload 0, ns_kernel MUON_NS_KERNEL_AUTO, ns_momentum_fused 1. */
+ * offload 0, ns_kernel MUON_NS_KERNEL_AUTO, ns_momentum_fused 1,
+ * ns_method MUON_NS_METHOD_STANDARD. */
 void muon_config_default(muon_config* cfg);
 
 /* Defines: "Muon Optimizer + FSDP", section 分块通信 (chunked communication:
@@ -137,7 +153,8 @@ void muon_config_default(muon_config* cfg);
  *           different labels never share a bucket.
  *   cfg:    NULL for muon_config_default.
  *   out:    receives the plan; free it with muon_plan_destroy.
- * Pure host work: needs no GPU.  Errors: MUON_ERR_INVALID. */
+ * Pure host work: needs no GPU.  Errors: MUON_ERR_INVALID; MUON_ERR_UNSUPPORTED when
+ * cfg->ns_method is GRAM and a bucket is not run by the small-matrix kernel. */
 muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t* groups,
                       int64_t bucket_cap_bytes, const muon_config* cfg, muon_plan_t** out);
 

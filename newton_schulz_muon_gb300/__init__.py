@@ -35,6 +35,8 @@ MUON_MOMENTUM_EMA = 0
 MUON_MOMENTUM_SGD = 1
 MUON_NS_KERNEL_AUTO = 0
 MUON_NS_KERNEL_GEMM = 1
+MUON_NS_METHOD_STANDARD = 0
+MUON_NS_METHOD_GRAM = 1
 MUON_MAX_NS_STEPS = 16
 
 
@@ -47,7 +49,8 @@ class muon_config(ctypes.Structure):
                 ("ns_precision", c_int32), ("momentum_form", c_int32), ("grad_dtype", c_int32),
                 ("param_dtype", c_int32), ("max_inflight", c_int32), ("skip_nonfinite", c_int32),
                 ("timing", c_int32), ("offload", c_int32), ("ns_kernel", c_int32),
-                ("offload_zero_copy", c_int32), ("ns_momentum_fused", c_int32), ("reserved", c_int32 * 1)]
+                ("offload_zero_copy", c_int32), ("ns_momentum_fused", c_int32), ("ns_method", c_int32),
+                ("reserved", c_int32 * 2)]
 
 
 class muon_plan_info(ctypes.Structure):

@@ -22,7 +22,8 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUD
 LIBMUON = os.path.join(PKG, "libmuon.so")
 LIBSYNTH = os.path.join(ROOT, "synth", "libmuonsynth.so")
 
-MUON_SOURCES = ["runtime.cu", "elementwise.cu", "ns_gemm.cu", "ns_small.cu", "noalloc.cu", "schedule.cu"]
+MUON_SOURCES = ["runtime.cu", "elementwise.cu", "ns_gemm.cu", "ns_small.cu", "ns_gram.cu", "noalloc.cu",
+                "schedule.cu"]
 
 
 def _nvcc() -> str:

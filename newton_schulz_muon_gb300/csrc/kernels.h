@@ -209,6 +209,8 @@ int gemm_max_clusters(bool tf32, int cluster, int num_sms);
 size_t gemm_smem_bytes(bool tf32);
 // All iterations of a bucket whose groups all have m <= 128 (bf16 only).
 cudaError_t launch_ns_small(const SmallArgs& a, int num_sms, cudaStream_t s);
+// The same by the gram method (the iteration on X X^T, X read twice).
+cudaError_t launch_ns_gram(const SmallArgs& a, int num_sms, cudaStream_t s);
 constexpr int kSmallMaxRows = 128;
 
 // Records `msg` as the calling thread's muon_last_error text and returns `s`.

@@ -666,7 +666,8 @@ muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cuda
       sa.pseg[i].norm_out = prep->seg[i].norm_out;
     }
   }
-  cudaError_t e = launch_ns_small(sa, p->num_sms, st);
+  cudaError_t e = p->cfg.ns_method == MUON_NS_METHOD_GRAM ? launch_ns_gram(sa, p->num_sms, st)
+                                                           : launch_ns_small(sa, p->num_sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "small-matrix Newton-Schulz launch");
   return MUON_OK;
 }
@@ -837,6 +838,8 @@ muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t*
     return fail(MUON_ERR_INVALID, "ns_kernel must be AUTO or GEMM");
   if (c.ns_momentum_fused != 0 && c.ns_momentum_fused != 1)
     return fail(MUON_ERR_INVALID, "ns_momentum_fused must be 0 or 1");
+  if (c.ns_method != MUON_NS_METHOD_STANDARD && c.ns_method != MUON_NS_METHOD_GRAM)
+    return fail(MUON_ERR_INVALID, "ns_method must be STANDARD or GRAM");
   muon_plan_t* p = new (std::nothrow) muon_plan_t();
   if (!p) return fail(MUON_ERR_INVALID, "out of host memory");
   static std::atomic<uint64_t> next_id{1};
@@ -844,6 +847,14 @@ muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t*
   p->cfg = c;
   p->cap = bucket_cap_bytes;
   muon_status s = build_plan(p, shapes, n_shapes, groups);
+  if (s == MUON_OK && c.ns_method == MUON_NS_METHOD_GRAM)
+    for (size_t b = 0; b < p->buckets.size(); ++b)
+      if (!uses_small_kernel(c, p->buckets[b])) {
+        s = fail(MUON_ERR_UNSUPPORTED,
+                 "the gram method runs in the small-matrix kernel only: bucket %zu has a matrix with "
+                 "min(rows, cols) > 128, or the configuration is not bf16 with ns_kernel AUTO", b);
+        break;
+      }
   if (s != MUON_OK) {
     delete p;
     return s;

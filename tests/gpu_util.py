@@ -117,7 +117,7 @@ class Workload:
 
 def check_step(wl: Workload, W_prev, M_prev, W_new, M_new, *, lr, mu, nesterov, wd, ns_steps,
                coeffs=oracle.DEFAULT_COEFFS, eps=1e-7, form="ema", tol=TOL_BF16, sample=None,
-               bf16_max_bound=None):
+               bf16_max_bound=None, method="standard"):
     """Teacher-forced comparison of one GPU step against the oracle, per logical matrix.
 
     W_prev/M_prev are the host copies of the state the GPU started from; W_new/M_new
@@ -136,7 +136,7 @@ def check_step(wl: Workload, W_prev, M_prev, W_new, M_new, *, lr, mu, nesterov, 
             Mp = M_prev[i][j]
             G = widen(wl.G[i][j], wl.g_dtype)
             Wo, Mo, U = oracle.muon_matrix_step(Wp, Mp, G, f32(lr), mu32, nesterov, f32(wd), ns_steps,
-                                                c32, f32(eps), form, one_minus_mu=omu)
+                                                c32, f32(eps), form, one_minus_mu=omu, method=method)
             ulp = int(ulp_distance(M_new[i][j], Mo).max())
             assert ulp <= 1, f"tensor {i} matrix {j}: momentum differs by {ulp} ulp"
             if wl.w_dtype == synth.BF16:
@@ -169,7 +169,7 @@ def bf16_weight_check(W_new_bits, Wo, Wp, tol, max_bound=None):
 
 def run_steps(m, wl, *, lr=0.02, mu=0.95, nesterov=True, wd=0.0, ns_steps=5, cap=512 << 20, cfg=None,
               steps=1, form="ema", coeffs=oracle.DEFAULT_COEFFS, sample=None, tol=TOL_BF16,
-              schedule=None, bf16_max_bound=None):
+              schedule=None, bf16_max_bound=None, method="standard"):
     """Run `steps` GPU Muon steps on a Workload, checking each against the oracle.
     ``schedule``: per-iteration (a, b, c) set on the plan (and used by the oracle)
     in place of ``coeffs``."""
@@ -198,7 +198,7 @@ def run_steps(m, wl, *, lr=0.02, mu=0.95, nesterov=True, wd=0.0, ns_steps=5, cap
         M_new = [to_numpy(t, synth.F32) for t in wl.dM]
         u, r = check_step(wl, W_prev, M_prev, W_new, M_new, lr=lr, mu=mu, nesterov=nesterov, wd=wd,
                           ns_steps=ns_steps, coeffs=coeffs, form=form, sample=sample, tol=tol,
-                          bf16_max_bound=bf16_max_bound)
+                          bf16_max_bound=bf16_max_bound, method=method)
         worst = (max(worst[0], u), max(worst[1], r))
     return worst
 

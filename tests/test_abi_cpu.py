@@ -198,3 +198,16 @@ def test_schedule_arguments_are_checked(nsm):
         assert e.value.status == nsm.MUON_ERR_INVALID
     assert nsm.lib.muon_set_ns_schedule(None, out, 1) == nsm.MUON_ERR_INVALID
     assert nsm.lib.muon_set_ns_schedule(p.handle, None, 2) == nsm.MUON_ERR_INVALID
+
+
+def test_gram_method_plans_only_small_matrix_buckets(nsm):
+    cfg = nsm.muon_config_default(ns_method=nsm.MUON_NS_METHOD_GRAM)
+    p = nsm.muon_plan([(128, 2560, 48), (700, 96)], config=cfg)      # every matrix has m <= 128
+    assert all(nsm.muon_get_bucket_info(p, b).ns_single_kernel for b in range(nsm.muon_get_plan_info(p).n_buckets))
+    for bad in ([(256, 512)], [(128, 512), (4096, 2560)]):
+        with pytest.raises(nsm.MuonError) as e:
+            nsm.muon_plan(bad, config=cfg)
+        assert e.value.status == nsm.MUON_ERR_UNSUPPORTED
+    with pytest.raises(nsm.MuonError) as e:
+        nsm.muon_plan([(128, 512)], config=nsm.muon_config_default(ns_method=2))
+    assert e.value.status == nsm.MUON_ERR_INVALID
