@@ -37,6 +37,8 @@ LR, MU, WD, NS_STEPS = 0.02, 0.95, 0.0, 5
 # Newton-Schulz coefficients: "fixed" (the configuration's (a, b, c) every
 # iteration) or "minimax" (per-iteration schedule, see --ns-schedule); set by main()
 NS_SCHEDULE = {"kind": "fixed", "lower": 1e-3, "safety": 1.05}
+# Newton-Schulz method: "standard" (the iteration on X) or "gram" (on X X^T); set by main()
+NS_METHOD = "standard"
 G_SIGMA, W_SIGMA, M_SIGMA = 1e-3, 0.02, 0.02
 
 
@@ -57,6 +59,13 @@ def ns_executed_flops(rows, cols, steps=None, bm=128, bn=256, bk=64, small=False
     steps = NS_STEPS if steps is None else steps
     m, n = min(rows, cols), max(rows, cols)
     cd = lambda a, b: -(-a // b)
+    if small and NS_METHOD == "gram":
+        # Gram and U = R X0 (high and low parts of R) over the chunks; per iteration
+        # A A, Q A, Q R and (Q A) Q as three bf16 products each (the last iteration
+        # skips Q A and (Q A) Q)
+        npad = cd(n, 128) * 128
+        sq = 3 * 2 * 128 ** 3
+        return 2 * 128 * 128 * npad + 2 * 2 * 128 * 128 * npad + sq * (4 * steps - 2)
     if small:
         npad = cd(n, 128) * 128
         return steps * (2 * 128 * 128 * npad + 2 * 128 ** 3 + 2 * 128 * 128 * npad)
@@ -137,14 +146,18 @@ def oracle_step(sample):
     import oracle
     co = oracle_coeffs()
     for W, M, G in sample:
-        oracle.muon_matrix_step(W, M, G, LR, MU, True, WD, NS_STEPS, co)
+        oracle.muon_matrix_step(W, M, G, LR, MU, True, WD, NS_STEPS, co, method=NS_METHOD)
 
 
 def schedule_config():
-    """The --ns-schedule choice as both arms state it in their config."""
+    """The --ns-schedule and --ns-method choices as both arms state them in their config."""
     if NS_SCHEDULE["kind"] != "minimax":
-        return {"kind": "fixed", "coeffs": [3.4445, -4.7750, 2.0315]}
-    return {"kind": "minimax", "lower": NS_SCHEDULE["lower"], "safety": NS_SCHEDULE["safety"]}
+        out = {"kind": "fixed", "coeffs": [3.4445, -4.7750, 2.0315]}
+    else:
+        out = {"kind": "minimax", "lower": NS_SCHEDULE["lower"], "safety": NS_SCHEDULE["safety"]}
+    if NS_METHOD != "standard":
+        out["method"] = NS_METHOD
+    return out
 
 
 def spec_bytes(spec):
@@ -387,6 +400,9 @@ def launches_per_step(nsm, plan, info, ns_only=False):
 
 def ns_kernel_name(nsm, plan, info):
     single = [nsm.muon_get_bucket_info(plan, b).ns_single_kernel for b in range(info.n_buckets)]
+    if all(single) and NS_METHOD == "gram":
+        return ("ns_gram_kernel (bf16 X, the iteration on X X^T with split-bf16 128x128 products, "
+                "X read twice, with the fused weight update)")
     if all(single):
         return "ns_small_kernel (bf16, every iteration in one launch, with the fused weight update)"
     if not any(single):
@@ -520,7 +536,9 @@ def run_gpu(args):
     tf32 = args.ns_precision == "tf32x3"
     cfg = nsm.muon_config_default(timing=1, grad_dtype=spec["g_dtype"], param_dtype=spec["w_dtype"],
                                   ns_precision=nsm.MUON_NS_TF32X3 if tf32 else nsm.MUON_NS_BF16,
-                                  ns_momentum_fused=1 if args.momentum == "fused" else 0)
+                                  ns_momentum_fused=1 if args.momentum == "fused" else 0,
+                                  ns_method=nsm.MUON_NS_METHOD_GRAM if NS_METHOD == "gram"
+                                  else nsm.MUON_NS_METHOD_STANDARD)
     plan = nsm.muon_plan(shapes, bucket_cap_bytes=spec["cap"], config=cfg)
     info = nsm.muon_get_plan_info(plan)
     momentum_fused = all(nsm.muon_get_bucket_info(plan, b).momentum_in_ns_kernel for b in range(info.n_buckets))
@@ -819,6 +837,8 @@ def main():
                     help="Newton-Schulz arithmetic: bf16 (default) or the 3xTF32 accuracy mode")
     ap.add_argument("--layers", type=int, default=None,
                     help="heads / experts: fewer layers than the full workload (profiling captures)")
+    ap.add_argument("--ns-method", choices=["standard", "gram"], default="standard",
+                    help="Newton-Schulz on X (standard) or on X X^T (gram: small-matrix buckets only, X read twice)")
     ap.add_argument("--momentum", choices=["fused", "separate"], default="fused",
                     help="small-matrix buckets: the momentum computed in the Newton-Schulz kernel's first pass "
                          "(default, the library's default), or the momentum kernel first")
@@ -830,8 +850,9 @@ def main():
     ap.add_argument("--ns-lower", type=float, default=1e-3, help="minimax: assumed lower end of the singular values")
     ap.add_argument("--ns-safety", type=float, default=1.05, help="minimax: widening of each fitted interval's top")
     args = ap.parse_args()
-    global NS_STEPS
+    global NS_STEPS, NS_METHOD
     NS_STEPS = args.ns_steps
+    NS_METHOD = args.ns_method
     NS_SCHEDULE.update(kind=args.ns_schedule, lower=args.ns_lower, safety=args.ns_safety)
     if args.warmup < 3:
         args.warmup = 3
