@@ -16,6 +16,8 @@ from typing import Optional, Sequence
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmuon.so")
+# the same library with the device range checks of the debug build (use_debug_library)
+LIB_PATH_DEBUG = os.path.join(_HERE, "libmuon_debug.so")
 
 # status codes, dtypes and enums of include/muon.h
 MUON_OK = 0
@@ -78,11 +80,11 @@ class muon_stats(ctypes.Structure):
                 ("h2d_bytes", c_int64), ("d2h_bytes", c_int64), ("n_buckets", c_int64)]
 
 
-def _load() -> ctypes.CDLL:
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libmuon.so not found at {LIB_PATH}; run __graft_entry__.build() "
+def _load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{os.path.basename(path)} not found at {path}; run __graft_entry__.build() "
                           "(there is no CPU fallback)")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     P = c_void_p
     sig = {
         "muon_config_default": (None, [POINTER(muon_config)]),
@@ -127,6 +129,14 @@ def _lib() -> ctypes.CDLL:
     if _LIB is None:
         _LIB = _load()
     return _LIB
+
+
+def use_debug_library(on: bool = True) -> None:
+    """Route every later call to libmuon_debug.so (device range checks that record
+    MUON_ERR_DEVICE instead of touching memory out of range) or back to libmuon.so.
+    A plan belongs to the library that made it: switch only when no plan is alive."""
+    global _LIB
+    _LIB = _load(LIB_PATH_DEBUG if on else LIB_PATH)
 
 
 def __getattr__(name):

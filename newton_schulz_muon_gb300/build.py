@@ -1,4 +1,5 @@
-"""Builds libmuon.so (the Muon step) and libmuonsynth.so (seeded input fill) in-tree.
+"""Builds libmuon.so (the Muon step), libmuon_debug.so (the same with the device
+range checks of -DMUON_DEBUG) and libmuonsynth.so (seeded input fill) in-tree.
 
 nvcc compiles each translation unit for sm_103a in parallel, then links a
 shared library next to the sources.  No CMake, no torch extension machinery.
@@ -20,6 +21,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
 LIBMUON = os.path.join(PKG, "libmuon.so")
+LIBMUON_DEBUG = os.path.join(PKG, "libmuon_debug.so")
 LIBSYNTH = os.path.join(ROOT, "synth", "libmuonsynth.so")
 
 MUON_SOURCES = ["runtime.cu", "elementwise.cu", "ns_gemm.cu", "ns_small.cu", "ns_gram.cu", "noalloc.cu",
@@ -52,14 +54,19 @@ def build(verbose: bool = False, force: bool = False) -> None:
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(INCLUDE, "muon.h"))
+    os.makedirs(os.path.join(BUILD, "debug"), exist_ok=True)
     jobs = []
-    objs = []
+    objs, dobjs = [], []
     for src in MUON_SOURCES:
         s = os.path.join(CSRC, src)
         o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        d = os.path.join(BUILD, "debug", src.replace(".cu", ".o"))
         objs.append(o)
+        dobjs.append(d)
         if force or not _newer(o, [s] + headers):
             jobs.append([nvcc, *ARCH, *COMMON, "-c", s, "-o", o])
+        if force or not _newer(d, [s] + headers):
+            jobs.append([nvcc, *ARCH, *COMMON, "-DMUON_DEBUG", "-c", s, "-o", d])
     synth_src = os.path.join(ROOT, "synth", "csrc", "synth.cu")
     synth_obj = os.path.join(BUILD, "synth.o")
     if force or not _newer(synth_obj, [synth_src]):
@@ -72,6 +79,8 @@ def build(verbose: bool = False, force: bool = False) -> None:
                 print(r.stdout + r.stderr, file=sys.stderr)
     if force or not _newer(LIBMUON, objs):
         _run([nvcc, *ARCH, "-shared", "-o", LIBMUON, *objs])
+    if force or not _newer(LIBMUON_DEBUG, dobjs):
+        _run([nvcc, *ARCH, "-shared", "-o", LIBMUON_DEBUG, *dobjs])
     if force or not _newer(LIBSYNTH, [synth_obj]):
         _run([nvcc, *ARCH, "-shared", "-o", LIBSYNTH, synth_obj])
 
@@ -79,4 +88,5 @@ def build(verbose: bool = False, force: bool = False) -> None:
 if __name__ == "__main__":
     build(verbose=True, force="--force" in sys.argv)
     print(LIBMUON)
+    print(LIBMUON_DEBUG)
     print(LIBSYNTH)

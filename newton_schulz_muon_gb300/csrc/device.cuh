@@ -11,10 +11,25 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "kernels.h"  // the device status word and its bits
+
 namespace muon {
 
-// Device status word bits (workspace offset 0).
-constexpr unsigned kStatusWaitTimeout = 1u;
+
+// Range checks of the debug build (-DMUON_DEBUG): a failed check records
+// kStatusGuard in the status word, raises the CTA's abort flag and returns false
+// so that the caller skips the access.  In the release build every check is
+// true at compile time.
+__device__ __forceinline__ bool guard_fail(unsigned* status, volatile int* abort) {
+  if (status != nullptr) atomicOr(status, kStatusGuard);
+  if (abort != nullptr) *abort = 1;
+  return false;
+}
+#ifdef MUON_DEBUG
+#define MUON_GUARD(cond, status, abort) ((cond) ? true : ::muon::guard_fail((status), (abort)))
+#else
+#define MUON_GUARD(cond, status, abort) true
+#endif
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 

@@ -17,9 +17,11 @@ constexpr int kPrepTile = 64;    // momentum / apply tiles are 64 x 64 elements
 
 // Workspace header (offset 0): device status word and non-finite counter.
 struct DeviceStatus {
-  unsigned flags;       // kStatusWaitTimeout, ...
+  unsigned flags;       // kStatusWaitTimeout, kStatusGuard
   unsigned nonfinite;   // matrices with a non-finite norm since the last muon_sync
 };
+constexpr unsigned kStatusWaitTimeout = 1u;  // a kernel's bounded wait ran out
+constexpr unsigned kStatusGuard = 2u;        // a debug-build range check failed; the access was skipped
 
 // ---------------------------------------------------------------------------
 // momentum + prep (one run of `count` matrices of one tensor)

@@ -1391,6 +1391,9 @@ muon_status muon_sync(muon_plan_t* p, void* stream, int64_t* n_nonfinite) {
   e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   if (n_nonfinite) *n_nonfinite = ds.nonfinite;
+  if (ds.flags & kStatusGuard)
+    return fail(MUON_ERR_DEVICE, "a device range check found an index out of range and skipped the access "
+                "(status 0x%x)", ds.flags);
   if (ds.flags) return fail(MUON_ERR_DEVICE, "a kernel gave up a bounded wait (status 0x%x)", ds.flags);
   if (ds.nonfinite) return MUON_WARN_NONFINITE;
   return MUON_OK;

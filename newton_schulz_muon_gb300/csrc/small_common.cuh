@@ -244,6 +244,13 @@ __device__ __forceinline__ const SmallPrepSeg& prep_seg(const SmallArgs& a, int 
   return a.pseg[lo];
 }
 
+// Debug build: an MMA operand tile of `bytes` at shared address `addr` lies inside
+// the CTA's dynamic shared memory [lo, hi).
+__device__ __forceinline__ bool smem_tile_ok(uint32_t addr, uint32_t bytes, uint32_t lo, uint32_t hi,
+                                             unsigned* status, volatile int* abort) {
+  return MUON_GUARD(addr >= lo && addr + bytes <= hi && (addr & 1023u) == 0, status, abort);
+}
+
 // Staging slot q % 4 of the fused momentum: slots 0 and 1 from slots01, 2 and 3
 // from slots23 (each pair 2 * kPrepSlot contiguous bytes).
 __device__ __forceinline__ uint8_t* prep_slot(uint8_t* slots01, uint8_t* slots23, int q) {
