@@ -24,6 +24,7 @@
 
 #include "device.cuh"
 #include "kernels.h"
+#include "epilogue.cuh"
 #include "momentum.cuh"
 
 namespace muon {
@@ -71,6 +72,9 @@ __device__ __forceinline__ void store_x(void* x_hi, float* x_lo, int64_t i, floa
   }
 }
 
+// Thread (tx, ty) of a 64 x 64 tile: rows ty and ty + 32, columns 8 tx .. 8 tx + 7,
+// so that a full tile of a matrix whose rows are whole 16-byte units moves with
+// 16-byte accesses (bf16 G and X0: one per row; fp32 M: two per row).
 __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_constant__ PrepArgs a) {
   __shared__ float vt[kT][kT + 1];
   __shared__ float red[kThreads / 32];
@@ -80,57 +84,67 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
   const PrepSeg& s = a.seg[tile.seg];
   const int64_t rows = s.rows, cols = s.cols;
   const int64_t base = tile.mat * s.stride;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int tx = threadIdx.x & 7, ty = threadIdx.x >> 3;
   const float mu = a.mu, omu = a.omu;
   float sumsq = 0.f;
-  float v[4][4];
+  float v[2][8];
 
   const bool full = (tile.r0 + kT <= rows) && (tile.c0 + kT <= cols);
-  const bool vec = full && ((cols & 3) == 0) && ((s.stride & 3) == 0);
+  const bool vec = full && ((cols & 7) == 0) && ((s.stride & 7) == 0);
   float* mrow = s.m + base;
   if (vec) {
-    // all loads of the thread's 4 x 4 elements first, then arithmetic, then stores
-    float4 mv[4];
-    float gv[4][4];
+    // all loads of the thread's 2 x 8 elements first, then arithmetic, then stores
+    float4 mv[2][2];
+    float gv[2][8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t off = (tile.r0 + ty + 16 * k) * cols + tile.c0 + 4 * tx;
-      mv[k] = __ldcs(reinterpret_cast<const float4*>(mrow + off));
+    for (int k = 0; k < 2; ++k) {
+      const int64_t off = (tile.r0 + ty + 32 * k) * cols + tile.c0 + 8 * tx;
+      mv[k][0] = __ldcs(reinterpret_cast<const float4*>(mrow + off));
+      mv[k][1] = __ldcs(reinterpret_cast<const float4*>(mrow + off + 4));
       if (a.grad_dtype == 1) {
-        const uint2 raw = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(s.g) + base + off));
-        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-        gv[k][0] = __low2float(g01); gv[k][1] = __high2float(g01);
-        gv[k][2] = __low2float(g23); gv[k][3] = __high2float(g23);
+        const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(s.g) + base + off));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+          gv[k][2 * h] = __low2float(p);
+          gv[k][2 * h + 1] = __high2float(p);
+        }
       } else {
-        const float4 f = __ldcs(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(s.g) + base + off));
-        gv[k][0] = f.x; gv[k][1] = f.y; gv[k][2] = f.z; gv[k][3] = f.w;
+        const float* gp = reinterpret_cast<const float*>(s.g) + base + off;
+        const float4 f0 = __ldcs(reinterpret_cast<const float4*>(gp));
+        const float4 f1 = __ldcs(reinterpret_cast<const float4*>(gp + 4));
+        gv[k][0] = f0.x; gv[k][1] = f0.y; gv[k][2] = f0.z; gv[k][3] = f0.w;
+        gv[k][4] = f1.x; gv[k][5] = f1.y; gv[k][6] = f1.z; gv[k][7] = f1.w;
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float mo[4] = {mv[k].x, mv[k].y, mv[k].z, mv[k].w};
-      float mn[4];
+    for (int k = 0; k < 2; ++k) {
+      const float mo[8] = {mv[k][0].x, mv[k][0].y, mv[k][0].z, mv[k][0].w,
+                           mv[k][1].x, mv[k][1].y, mv[k][1].z, mv[k][1].w};
+      float mn[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         mn[j] = dot2_accurate(mu, mo[j], omu, gv[k][j]);
         v[k][j] = nesterov_input(a.nesterov, mu, mn[j], omu, gv[k][j]);
         sumsq = __fmaf_rn(v[k][j], v[k][j], sumsq);
       }
-      mv[k] = make_float4(mn[0], mn[1], mn[2], mn[3]);
+      mv[k][0] = make_float4(mn[0], mn[1], mn[2], mn[3]);
+      mv[k][1] = make_float4(mn[4], mn[5], mn[6], mn[7]);
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t off = (tile.r0 + ty + 16 * k) * cols + tile.c0 + 4 * tx;
-      __stcs(reinterpret_cast<float4*>(mrow + off), mv[k]);
+    for (int k = 0; k < 2; ++k) {
+      const int64_t off = (tile.r0 + ty + 32 * k) * cols + tile.c0 + 8 * tx;
+      __stcs(reinterpret_cast<float4*>(mrow + off), mv[k][0]);
+      __stcs(reinterpret_cast<float4*>(mrow + off + 4), mv[k][1]);
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t r = tile.r0 + ty + 16 * k;
-      const int64_t c = tile.c0 + 4 * tx;
+    for (int k = 0; k < 2; ++k) {
+      const int64_t r = tile.r0 + ty + 32 * k;
+      const int64_t c = tile.c0 + 8 * tx;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         v[k][j] = 0.f;
         if (r < rows && c + j < cols) {
           const int64_t off = r * cols + c + j;
@@ -150,27 +164,24 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
   const bool need_vt = s.transposed || a.tf32;
   if (need_vt) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < 2; ++k)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) vt[ty + 16 * k][4 * tx + j] = v[k][j];
+      for (int j = 0; j < 8; ++j) vt[ty + 32 * k][8 * tx + j] = v[k][j];
     __syncthreads();
   }
   // P[r][c] = V[r][c]
   auto store_direct = [&](void* hi, float* lo, int64_t ld, int64_t base) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t r = tile.r0 + ty + 16 * k;
-      const int64_t c = tile.c0 + 4 * tx;
-      if (full && !a.tf32) {
-        __nv_bfloat162 p0 = __floats2bfloat162_rn(v[k][0], v[k][1]);
-        __nv_bfloat162 p1 = __floats2bfloat162_rn(v[k][2], v[k][3]);
-        uint2 raw;
-        raw.x = *reinterpret_cast<uint32_t*>(&p0);
-        raw.y = *reinterpret_cast<uint32_t*>(&p1);
-        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(hi) + base + r * ld + c) = raw;
+    for (int k = 0; k < 2; ++k) {
+      const int64_t r = tile.r0 + ty + 32 * k;
+      const int64_t c = tile.c0 + 8 * tx;
+      if (full && !a.tf32 && (ld & 7) == 0) {
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(hi) + base + r * ld + c) =
+            make_uint4(pack_bf16x2(v[k][0], v[k][1]), pack_bf16x2(v[k][2], v[k][3]),
+                       pack_bf16x2(v[k][4], v[k][5]), pack_bf16x2(v[k][6], v[k][7]));
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 8; ++j)
           if (r < rows && c + j < cols) store_x(hi, lo, base + r * ld + c + j, v[k][j], a.tf32);
       }
     }
@@ -178,24 +189,21 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
   // P[c][r] = V[r][c]: P row = source column, P column = source row
   auto store_transposed = [&](void* hi, float* lo, int64_t ld, int64_t base) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int xi = ty + 16 * k;
+    for (int k = 0; k < 2; ++k) {
+      const int xi = ty + 32 * k;
       const int64_t xr = tile.c0 + xi;
-      const int64_t xc = tile.r0 + 4 * tx;
-      float w4[4];
+      const int64_t xc = tile.r0 + 8 * tx;
+      float w8[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) w4[j] = vt[4 * tx + j][xi];
-      if (full && !a.tf32) {
-        __nv_bfloat162 p0 = __floats2bfloat162_rn(w4[0], w4[1]);
-        __nv_bfloat162 p1 = __floats2bfloat162_rn(w4[2], w4[3]);
-        uint2 raw;
-        raw.x = *reinterpret_cast<uint32_t*>(&p0);
-        raw.y = *reinterpret_cast<uint32_t*>(&p1);
-        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(hi) + base + xr * ld + xc) = raw;
+      for (int j = 0; j < 8; ++j) w8[j] = vt[8 * tx + j][xi];
+      if (full && !a.tf32 && (ld & 7) == 0) {
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(hi) + base + xr * ld + xc) =
+            make_uint4(pack_bf16x2(w8[0], w8[1]), pack_bf16x2(w8[2], w8[3]),
+                       pack_bf16x2(w8[4], w8[5]), pack_bf16x2(w8[6], w8[7]));
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (xr < cols && xc + j < rows) store_x(hi, lo, base + xr * ld + xc + j, w4[j], a.tf32);
+        for (int j = 0; j < 8; ++j)
+          if (xr < cols && xc + j < rows) store_x(hi, lo, base + xr * ld + xc + j, w8[j], a.tf32);
       }
     }
   };

@@ -402,22 +402,24 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
   const uint32_t tmem_base = tmem_slot;
   const int mode = a.mode;
   const bool mn_b = (mode == kUpdate) && !kTF32;  // B operand read MN-major
-  // This cluster's tiles: sched_units[s_begin .. s_end).  The schedule lives in the
-  // caller's workspace; the debug build checks it before any role uses it (every
-  // thread reaches the same verdict), and on a bad entry the cluster runs nothing.
-  int s_begin = a.sched_off[cluster_id], s_end = a.sched_off[cluster_id + 1];
 #ifdef MUON_DEBUG
+  // Debug build: the tile schedule lives in the caller's workspace; every thread
+  // checks this cluster's range of it (offsets in order and within the tile count,
+  // every tile index in range) before any role uses it, and on a bad entry no role
+  // runs a tile.  The release build leaves these loops exactly as they are.
+  bool sched_ok;
   {
-    bool sched_ok = cluster_id < a.n_clusters && 0 <= s_begin && s_begin <= s_end && s_end <= a.total_tiles;
-    for (int si = s_begin; sched_ok && si < s_end; ++si) {
+    const int lo = a.sched_off[cluster_id], hi = a.sched_off[cluster_id + 1];
+    sched_ok = cluster_id < a.n_clusters && 0 <= lo && lo <= hi && hi <= a.total_tiles;
+    for (int si = lo; sched_ok && si < hi; ++si) {
       const int t = a.sched_units[si];
       sched_ok = 0 <= t && t < a.total_tiles;
     }
-    if (!sched_ok) {
-      if (threadIdx.x == 0) guard_fail(status, abort_p);
-      s_begin = s_end = 0;
-    }
+    if (!sched_ok && threadIdx.x == 0) guard_fail(status, abort_p);
   }
+#define MUON_SCHED_OK sched_ok &&
+#else
+#define MUON_SCHED_OK
 #endif
 
   if (warp == 0) {
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     // Issuing from a lone lane of a diverged warp is several times slower.
     int stage = 0;
     uint32_t phase = 0;
-    for (int si = s_begin; si < s_end; ++si) {
+    for (int si = a.sched_off[cluster_id]; MUON_SCHED_OK si < a.sched_off[cluster_id + 1]; ++si) {
       const int t = a.sched_units[si];
       const TileCoord tc = decode_tile<kCL>(a, t, rank);
       const GemmGroup& G = a.g[tc.g];
@@ -491,8 +493,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int si = s_begin; si < s_end; ++si) {
-        const int t = a.sched_units[si];
+      for (int si = a.sched_off[cluster_id]; MUON_SCHED_OK si < a.sched_off[cluster_id + 1]; ++si) {
+      const int t = a.sched_units[si];
         const TileCoord tc = decode_tile<kCL>(a, t, rank);
         const GemmGroup& G = a.g[tc.g];
         const int kblocks = (G.K + C::kBK - 1) / C::kBK;
@@ -505,11 +507,16 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
           // the TMA bytes are visible to the tensor core once the barrier completes
           const bool got = mbar_wait(&full_bar[stage], phase, abort_p, status);
           if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+#ifdef MUON_DEBUG
           // debug build: the stage's operands lie inside the ring, the accumulator in
           // the allocated Tensor Memory columns
-          const bool in_range =
-              MUON_GUARD(stage >= 0 && stage < C::kStages && (uint32_t)(acc + 1) * kBN <= kTmemCols, status, abort_p);
-          if (lane == 0 && in_range) {
+          if (!(stage >= 0 && stage < C::kStages && (uint32_t)(acc + 1) * kBN <= kTmemCols)) {
+            guard_fail(status, abort_p);
+            ok = false;
+            break;
+          }
+#endif
+          if (lane == 0) {
             const uint32_t sa = smem_u32(smem + (size_t)stage * C::kStage);
             const uint32_t sb = sa + C::kParts * C::kA;
 #pragma unroll
@@ -568,6 +575,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     uint64_t* dbar = &addend_bar[2 * ew];
     const uint32_t tempty_lead[2] = {kCL > 1 ? mapa_shared(&tempty_bar[0], 0) : 0u,
                                      kCL > 1 ? mapa_shared(&tempty_bar[1], 0) : 0u};
+    const int s_end = a.sched_off[cluster_id + 1];
     // addend chunks are requested in the order they are used, one ahead, across
     // tiles: request q lands in slot q % 2 and completes phase (q / 2) % 2
     const bool has_d = !kTF32 && mode == kPoly;
@@ -588,7 +596,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gemm_kernel(const __grid_cons
     int acc = 0;
     uint32_t acc_phase = 0;
     bool failed = false;
-    for (int si = s_begin; si < s_end && !failed; ++si) {
+    for (int si = a.sched_off[cluster_id]; MUON_SCHED_OK si < s_end && !failed; ++si) {
       const int t = a.sched_units[si];
       const TileCoord tc = decode_tile<kCL>(a, t, rank);
       const GemmGroup& G = a.g[tc.g];
@@ -879,5 +887,7 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, bool tf32, int cluster, 
   if (cluster == 2) return tf32 ? launch_impl<true, 2>(a, num_sms, s) : launch_impl<false, 2>(a, num_sms, s);
   return tf32 ? launch_impl<true, 1>(a, num_sms, s) : launch_impl<false, 1>(a, num_sms, s);
 }
+
+#undef MUON_SCHED_OK
 
 }  // namespace muon
