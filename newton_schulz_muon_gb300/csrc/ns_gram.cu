@@ -218,15 +218,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gram_kernel(const __grid_cons
     uint32_t ar = 0, qr = 0, pr = 0, rr = 0;
     uint32_t uc = 0;
     bool ok = true;
+#ifdef MUON_DEBUG
     const uint32_t smem_lo = smem_u32(smem), smem_hi = smem_lo + 7 * kUnit;
+#endif
     // Y Z^T from the rows of two split tiles, accumulated from zero into `acc`
     auto yzt = [&](uint32_t acc, uint32_t yh, uint32_t yl, uint32_t zh, uint32_t zl) {
+#ifdef MUON_DEBUG
       if (!(smem_tile_ok(yh, kUnit, smem_lo, smem_hi, status, abort_p) &&
             smem_tile_ok(yl, kUnit, smem_lo, smem_hi, status, abort_p) &&
             smem_tile_ok(zh, kUnit, smem_lo, smem_hi, status, abort_p) &&
             smem_tile_ok(zl, kUnit, smem_lo, smem_hi, status, abort_p) &&
             MUON_GUARD(acc + 128u <= kTmemColsG, status, abort_p)))
         return;
+#endif
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) mma<false, 1>(tmem + acc, tile_desc(yh, kk), tile_desc(zh, kk), idesc_sq, kk ? 1u : 0u);
 #pragma unroll
@@ -315,8 +319,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gram_kernel(const __grid_cons
         const int ub = (int)(uc % kUBufsG);
         if (poll(&full_bar[stage], phase) && poll(&u_empty[ub], ((uc / kUBufsG) & 1u) ^ 1u)) {
           tc_fence_after();
-          if (lane == 0 && smem_tile_ok(smem_u32(ring + (size_t)stage * kChunk), kChunk, smem_lo, smem_hi, status,
-                                        abort_p)) {
+#ifdef MUON_DEBUG
+          const bool stage_ok = smem_tile_ok(smem_u32(ring + (size_t)stage * kChunk), kChunk, smem_lo, smem_hi, status,
+                                             abort_p);
+#else
+          const bool stage_ok = true;
+#endif
+          if (lane == 0 && stage_ok) {
             const uint32_t xb = smem_u32(ring + (size_t)stage * kChunk);
             const uint32_t acc = tmem + (uint32_t)ub * 128u;
 #pragma unroll

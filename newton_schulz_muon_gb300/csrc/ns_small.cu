@@ -292,9 +292,13 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
       return smem_desc_sw128(base + (uint32_t)(kk >> 2) * kTile + (uint32_t)(kk & 3) * 32u, 16, 1024);
     };
     // X X^T over one 128-column tile (both operands: its rows, K-major)
+#ifdef MUON_DEBUG
     const uint32_t smem_lo = smem_u32(smem), smem_hi = smem_lo + (uint32_t)(kSmemS - 1024);
+#endif
     auto gram_tile = [&](uint32_t base, bool first) {
+#ifdef MUON_DEBUG
       if (!smem_tile_ok(base, kChunk, smem_lo, smem_hi, status, abort_p)) return;
+#endif
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint64_t d = sq_desc(base, kk);
