@@ -839,9 +839,9 @@ def main():
                     help="heads / experts: fewer layers than the full workload (profiling captures)")
     ap.add_argument("--ns-method", choices=["standard", "gram"], default="standard",
                     help="Newton-Schulz on X (standard) or on X X^T (gram: small-matrix buckets only, X read twice)")
-    ap.add_argument("--momentum", choices=["fused", "separate"], default="fused",
-                    help="small-matrix buckets: the momentum computed in the Newton-Schulz kernel's first pass "
-                         "(default, the library's default), or the momentum kernel first")
+    ap.add_argument("--momentum", choices=["separate", "fused"], default="separate",
+                    help="small-matrix buckets: the momentum kernel first (default, the library's default), or "
+                         "the momentum computed in the Newton-Schulz kernel's first pass")
     ap.add_argument("--offload-mode", choices=["copy", "zerocopy"], default="copy",
                     help="offload workload: staged copies (default) or zero-copy kernel access to host memory")
     ap.add_argument("--ns-steps", type=int, default=5, help="Newton-Schulz iterations per step (default 5)")

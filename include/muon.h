@@ -132,7 +132,7 @@ typedef struct {
 
 /* Fills *cfg with (3.4445, -4.7750, 2.0315), eps 1e-7, bf16 NS, EMA momentum,
  * bf16 gradients, fp32 weights, max_inflight 1, skip_nonfinite 1, timing 0,
- * offload 0, ns_kernel MUON_NS_KERNEL_AUTO, ns_momentum_fused 1,
+ * offload 0, ns_kernel MUON_NS_KERNEL_AUTO, ns_momentum_fused 0,
  * ns_method MUON_NS_METHOD_STANDARD. */
 void muon_config_default(muon_config* cfg);
 

@@ -813,7 +813,7 @@ void muon_config_default(muon_config* cfg) {
   cfg->timing = 0;
   cfg->offload = 0;
   cfg->ns_kernel = MUON_NS_KERNEL_AUTO;
-  cfg->ns_momentum_fused = 1;
+  cfg->ns_momentum_fused = 0;
 }
 
 muon_status muon_plan(const muon_shape* shapes, int32_t n_shapes, const int32_t* groups, int64_t bucket_cap_bytes,

@@ -39,6 +39,7 @@ def test_config_default(nsm):
     assert c.grad_dtype == nsm.MUON_DTYPE_BF16 and c.param_dtype == nsm.MUON_DTYPE_F32
     assert c.max_inflight == 1 and c.skip_nonfinite == 1 and c.offload == 0
     assert c.ns_kernel == nsm.MUON_NS_KERNEL_AUTO
+    assert c.ns_momentum_fused == 0 and c.ns_method == nsm.MUON_NS_METHOD_STANDARD
 
 
 QWEN3_4B_LAYER = [(4096, 2560), (1024, 2560), (1024, 2560), (2560, 4096),

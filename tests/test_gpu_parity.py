@@ -456,18 +456,19 @@ def test_resume_from_copied_state_is_bitwise_identical(m):
 
 # --- metrics: per-bucket records and input norms ("Muon Optimizer + FSDP", 需要记录的指标) ---
 
-@pytest.mark.parametrize("g_dtype", [synth.BF16, synth.F32])
-def test_input_norms_match_the_oracle(m, g_dtype):
+@pytest.mark.parametrize("g_dtype,fused", [(synth.BF16, 1), (synth.BF16, 0), (synth.F32, 0)])
+def test_input_norms_match_the_oracle(m, g_dtype, fused):
     # ||V||_F of every matrix, tensor order: grouped-GEMM buckets, small-matrix
-    # buckets (bf16 gradients: the norm is summed inside the small kernel; fp32:
-    # by the momentum kernel), a tall matrix; a NaN matrix reports a non-finite norm
+    # buckets (with the momentum in the small kernel the norm is summed there;
+    # otherwise by the momentum kernel), a tall matrix; a NaN matrix reports a
+    # non-finite norm
     import math
     wl = Workload([(256, 512), (128, 640, 3), (700, 96), (64, 128, 2)], m_sigma=0.02, g_sigma=1e-3,
                   g_dtype=g_dtype)
     g = wl.dG[3].clone()
     g[1, 2, 3] = float("nan")
     plan = m.muon_plan(wl.plan_shapes(), bucket_cap_bytes=300_000,
-                       config=m.muon_config_default(grad_dtype=g_dtype))
+                       config=m.muon_config_default(grad_dtype=g_dtype, ns_momentum_fused=fused))
     assert m.muon_get_plan_info(plan).n_buckets >= 3
     m.allocate_workspace(plan)
     m.muon_step(plan, wl.dW, wl.dG[:3] + [g], wl.dM, 0.02, 0.95, True, 0.0, 5)
