@@ -354,25 +354,47 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-# DRAM bytes (read + write) per ns_gemm launch on the default workload, averaged
-# over the 15 launches of one step, from one ncu capture (the command and the
-# per-launch table are in profiles/ns_gemm_qwen3_4b_layer.md).  Valid only for the
-# kernel sources it was taken on: the bench reports null once their digest moves.
-NS_GEMM_TRAFFIC = {"bytes_per_launch": 348.4e6, "sources_sha256_16": "cd159d403de38d75"}
-KERNEL_SOURCES = ("newton_schulz_muon_gb300/csrc/ns_gemm.cu", "newton_schulz_muon_gb300/csrc/device.cuh",
-                  "newton_schulz_muon_gb300/csrc/kernels.h", "newton_schulz_muon_gb300/csrc/epilogue.cuh")
+# DRAM bytes (read + write) per launch from one ncu capture each, valid only for the
+# kernel sources they were taken on (the bench reports null once their digest
+# moves).  The commands and per-launch tables are in profiles/.
+#  - ns_gemm on the default workload: the mean over the 15 launches of one step
+#    (profiles/ns_gemm_qwen3_4b_layer.md).
+#  - the small-matrix kernels on 128 x 2560 heads (momentum kernel first): one
+#    launch over 7 layers (336 matrices), per matrix; a full launch scales by the
+#    matrices it holds (profiles/ns_gram_per_head_qkv.md, ns_small_per_head_qkv.md).
+GEMM_SOURCES = ['newton_schulz_muon_gb300/csrc/ns_gemm.cu', 'newton_schulz_muon_gb300/csrc/device.cuh', 'newton_schulz_muon_gb300/csrc/kernels.h', 'newton_schulz_muon_gb300/csrc/epilogue.cuh']
+GRAM_SOURCES = ['newton_schulz_muon_gb300/csrc/ns_gram.cu', 'newton_schulz_muon_gb300/csrc/small_common.cuh', 'newton_schulz_muon_gb300/csrc/device.cuh', 'newton_schulz_muon_gb300/csrc/kernels.h', 'newton_schulz_muon_gb300/csrc/epilogue.cuh', 'newton_schulz_muon_gb300/csrc/momentum.cuh']
+SMALL_SOURCES = ['newton_schulz_muon_gb300/csrc/ns_small.cu', 'newton_schulz_muon_gb300/csrc/small_common.cuh', 'newton_schulz_muon_gb300/csrc/device.cuh', 'newton_schulz_muon_gb300/csrc/kernels.h', 'newton_schulz_muon_gb300/csrc/epilogue.cuh', 'newton_schulz_muon_gb300/csrc/momentum.cuh']
+NS_GEMM_TRAFFIC = {"bytes_per_launch": 346.9e6, "sources_sha256_16": "9940b3a8090a4f28"}
+HEAD_TRAFFIC = {
+    "gram": {"bytes_per_matrix": (854.2e6 + 386.6e6) / 336, "sources_sha256_16": "8454c4b5272221c8"},
+    "standard": {"bytes_per_matrix": (880.5e6 + 748.4e6) / 336, "sources_sha256_16": "011243bf1e9f7d91"},
+}
 
 
-def ns_gemm_traffic():
+def sources_digest(files):
     import hashlib
     h = hashlib.sha256()
     root = os.path.dirname(os.path.abspath(__file__))
-    for f in KERNEL_SOURCES:
+    for f in files:
         with open(os.path.join(root, f), "rb") as fh:
             h.update(fh.read())
-    if h.hexdigest()[:16] != NS_GEMM_TRAFFIC["sources_sha256_16"]:
+    return h.hexdigest()[:16]
+
+
+def ns_gemm_traffic():
+    if sources_digest(GEMM_SOURCES) != NS_GEMM_TRAFFIC["sources_sha256_16"]:
         return None
     return NS_GEMM_TRAFFIC["bytes_per_launch"]
+
+
+def head_traffic(method, n_matrices):
+    """DRAM bytes of one small-matrix launch over n 128 x 2560 heads (momentum kernel
+    first), scaled from the 7-layer capture; None once the kernel's sources moved."""
+    t = HEAD_TRAFFIC[method]
+    if sources_digest(GRAM_SOURCES if method == "gram" else SMALL_SOURCES) != t["sources_sha256_16"]:
+        return None
+    return t["bytes_per_matrix"] * n_matrices
 
 
 def load_peaks():
@@ -422,14 +444,18 @@ def choose_bf16_peak(peaks, peak_kind, clocks, timed_s):
     return peaks["bf16_tflops"], f"{peak_kind} bf16 burst (no power cap seen, timed region {timed_s:.2f} s)"
 
 
-def ns_compulsory_bytes(tensors, w_sizes, g_sizes, momentum_fused):
+def ns_compulsory_bytes(tensors, w_sizes, g_sizes, momentum_fused, method="standard"):
     """Bytes the single-launch small-matrix kernel must move through HBM: the
     weights read and written once, plus X0 read once (bf16) or, when the kernel
-    computes the momentum itself, G read once and M read and written once."""
+    computes the momentum itself, G read once and M read and written once.  The
+    gram method reads X0 a second time for U = R X0 (and, computing the momentum
+    itself, writes X0 once for that)."""
     total = 0
     for (r, c, k), ws, gs in zip(tensors, w_sizes, g_sizes):
         e = k * r * c
         total += 2 * e * ws + (e * (gs + 8) if momentum_fused else e * 2)
+        if method == "gram":
+            total += e * (4 if momentum_fused else 2)
     return total
 
 
@@ -447,7 +473,8 @@ def tf32_peak(bf16_peak):
 
 
 def roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, executed, ns_bytes,
-                   peak_tf, peak_name, peaks, bf16_sustained, traffic):
+                   peak_tf, peak_name, peaks, bf16_sustained, traffic,
+                   bytes_counted="compulsory bytes: inputs read once, weights read and written once"):
     """The roofline object of the Newton-Schulz phase's dominant kernel, per launch.
 
     A tensor-bound kernel is measured on the flops its tensor cores execute (whole
@@ -466,7 +493,7 @@ def roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorit
                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic,
                     "peak_kind": "measured HBM copy bandwidth",
                     "algorithmic_bytes_per_launch": ns_bytes / ns_launches,
-                    "bytes_counted": "compulsory bytes: inputs read once, weights read and written once",
+                    "bytes_counted": bytes_counted,
                     "tensor_frac": exe_tf / peak_tf, "tensor_frac_algorithmic": alg_tf / peak_tf,
                     "tensor_peak_kind": peak_name})
     else:
@@ -616,7 +643,7 @@ def run_gpu(args):
     # L2 at best): when those bytes take longer at the HBM peak than the products
     # at the tensor peak, HBM is its roofline
     ns_bytes = ns_compulsory_bytes(tensors, [W[i].element_size() for i in range(len(tensors))],
-                                   [G[i].element_size() for i in range(len(tensors))], momentum_fused)
+                                   [G[i].element_size() for i in range(len(tensors))], momentum_fused, NS_METHOD)
     hbm_bound = single_kernel and not tf32 and hbm_binds(ns_bytes, algorithmic, peaks["hbm_gbs"], peak_tf)
 
     # ---- end to end through the C ABI with host buffers ----
@@ -706,7 +733,15 @@ def run_gpu(args):
                              "prep_frac": prep_bytes / (prep_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}),
         "roofline": roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, executed,
                                    ns_bytes, peak_tf, peak_name, peaks, bf16_sustained,
-                                   ns_gemm_traffic() if args.workload == "layer" and not tf32 else None),
+                                   ns_gemm_traffic() if args.workload == "layer" and not tf32 else
+                                   head_traffic(NS_METHOD, n_mats) if args.workload == "heads" and not momentum_fused
+                                   and NS_STEPS == 5 else None,
+                                   ("algorithmic bytes: " + ("G read, M read and written" if momentum_fused
+                                                             else "X0 read") +
+                                    (", X0 written and read back once more for U = R X0" if momentum_fused and
+                                     NS_METHOD == "gram" else ", X0 read again for U = R X0"
+                                     if NS_METHOD == "gram" else "") +
+                                    ", weights read and written once")),
         "clocks": clocks,
         "gpu_launches": args.steps * launches_per_step(nsm, plan, info),
     }

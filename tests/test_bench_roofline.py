@@ -144,3 +144,20 @@ def test_launches_per_step():
     nsm = Nsm([(0, 0), (1, 0), (1, 1)])   # GEMM bucket; small kernel after the momentum kernel; fused
     assert bench.launches_per_step(nsm, None, Info()) == (2 + 15) + (2 + 1) + 1
     assert bench.launches_per_step(nsm, None, Info(), ns_only=True) == 15 + 1 + 1
+
+
+def test_compulsory_bytes_of_the_gram_kernel():
+    # the gram method reads X0 twice (the Gram, then U = R X0): 12 B per element with
+    # the momentum kernel first; computing the momentum itself it writes X0 once and
+    # reads it back: G 2 + M 8 + X0 4 + W 8 = 22
+    t = [(128, 2560, 1728)]
+    e = 128 * 2560 * 1728
+    assert bench.ns_compulsory_bytes(t, [4], [2], False, "gram") == 12 * e
+    assert bench.ns_compulsory_bytes(t, [4], [2], True, "gram") == 22 * e
+
+
+def test_head_traffic_scales_by_matrices():
+    if bench.head_traffic("gram", 336) is None:
+        pytest.skip("the gram kernel's sources changed since the capture")
+    assert bench.head_traffic("gram", 336) == pytest.approx(854.2e6 + 386.6e6)
+    assert bench.head_traffic("gram", 1728) == pytest.approx((854.2e6 + 386.6e6) * 1728 / 336)
