@@ -566,7 +566,8 @@ def run_gpu(args):
                                   ns_momentum_fused=1 if args.momentum == "fused" else 0,
                                   ns_method=nsm.MUON_NS_METHOD_GRAM if NS_METHOD == "gram"
                                   else nsm.MUON_NS_METHOD_STANDARD)
-    plan = nsm.muon_plan(shapes, bucket_cap_bytes=spec["cap"], config=cfg)
+    cap = spec["cap"] if args.bucket_cap_mib is None else int(args.bucket_cap_mib) << 20
+    plan = nsm.muon_plan(shapes, bucket_cap_bytes=cap, config=cfg)
     info = nsm.muon_get_plan_info(plan)
     momentum_fused = all(nsm.muon_get_bucket_info(plan, b).momentum_in_ns_kernel for b in range(info.n_buckets))
     ws = nsm.allocate_workspace(plan)
@@ -718,7 +719,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "tf32x3" if tf32 else "bf16", "data": "synthetic",
         "config": arm_config(spec, world),
-        "plan": {"buckets": int(info.n_buckets), "ns_schedule_detail": schedule,
+        "plan": {"buckets": int(info.n_buckets), "bucket_cap_bytes": cap, "ns_schedule_detail": schedule,
                  "momentum_in_ns_kernel": momentum_fused},
         "ns_tflops": {"nominal": nominal / (ms * 1e-3) / 1e12, "algorithmic_in_ns_phase": ns_alg_tflops,
                       "executed_in_ns_phase": executed / (ns_ms * 1e-3) / 1e12,
@@ -872,6 +873,8 @@ def main():
                     help="Newton-Schulz arithmetic: bf16 (default) or the 3xTF32 accuracy mode")
     ap.add_argument("--layers", type=int, default=None,
                     help="heads / experts: fewer layers than the full workload (profiling captures)")
+    ap.add_argument("--bucket-cap-mib", type=int, default=None,
+                    help="micro-bucket cap in MiB of wide-form bf16 matrix bytes (default: the workload's own)")
     ap.add_argument("--ns-method", choices=["standard", "gram"], default="standard",
                     help="Newton-Schulz on X (standard) or on X X^T (gram: small-matrix buckets only, X read twice)")
     ap.add_argument("--momentum", choices=["separate", "fused"], default="separate",
