@@ -131,12 +131,20 @@ def _lib() -> ctypes.CDLL:
     return _LIB
 
 
+_LIB_DEBUG = False
+
+
 def use_debug_library(on: bool = True) -> None:
     """Route every later call to libmuon_debug.so (device range checks that record
     MUON_ERR_DEVICE instead of touching memory out of range) or back to libmuon.so.
     A plan belongs to the library that made it: switch only when no plan is alive."""
-    global _LIB
+    global _LIB, _LIB_DEBUG
     _LIB = _load(LIB_PATH_DEBUG if on else LIB_PATH)
+    _LIB_DEBUG = bool(on)
+
+
+def using_debug_library() -> bool:
+    return _LIB is not None and _LIB_DEBUG
 
 
 def __getattr__(name):

@@ -17,9 +17,14 @@ TOL_BF16_W = 3.5e-2
 
 
 def nsm():
+    """The binding, built; with MUON_TEST_DEBUG_LIB=1 in the environment every test
+    runs against the debug build (device range checks) instead."""
+    import os
     import newton_schulz_muon_gb300.build as b
     b.build()
     import newton_schulz_muon_gb300 as m
+    if os.environ.get("MUON_TEST_DEBUG_LIB") == "1" and m._LIB is None:
+        m.use_debug_library(True)
     return m
 
 

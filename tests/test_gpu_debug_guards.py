@@ -22,11 +22,12 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module")
 def m():
     mod = nsm()
-    gc.collect()                     # no plan of the release library is alive
+    was_debug = mod.using_debug_library()
+    gc.collect()                     # no plan of the other library is alive
     mod.use_debug_library(True)
     yield mod
     gc.collect()                     # the debug library's plans go before it does
-    mod.use_debug_library(False)
+    mod.use_debug_library(was_debug)
 
 
 @pytest.mark.parametrize("shapes,kw", [
