@@ -203,7 +203,7 @@ def set_schedule(nsm, plan):
 CPU_SAMPLE = {"layer": 7, "single": 1, "heads": 64, "experts": 16, "offload": 7}
 
 
-def cpu_baseline_leg(name, min_seconds=3.0):
+def cpu_baseline_leg(name, min_seconds=10.0):
     spec = workload_spec("layer" if name == "offload" else name)
     sample = oracle_sample(spec, CPU_SAMPLE[name])
     reps, dt = 0, 0.0
@@ -466,10 +466,39 @@ def hbm_binds(nbytes, flops, hbm_gbs, tensor_tflops):
 
 
 def tf32_peak(bf16_peak):
-    """The 3xTF32 mode's denominator: kind::tf32 products run at half the kind::f16
-    rate per SM on this part (a probe measured 4096 flop/clk/SM against 8192), so
-    the measured bf16 figure times 0.5."""
+    """The 3xTF32 mode's fallback denominator: kind::tf32 products run at half the
+    kind::f16 rate per SM on this part (a probe measured 4096 flop/clk/SM against
+    8192), so the measured bf16 figure times 0.5."""
     return 0.5 * bf16_peak
+
+
+def measure_tf32_gemm_tflops(n=8192, iters=20):
+    """cuBLAS's tf32 GEMM rate on this GPU, timed in this run: torch.matmul of two
+    n x n fp32 matrices with TF32 tensor cores allowed, CUDA events around `iters`
+    products after three warm-up ones.  It is measured like the bf16 figure of the
+    peaks file (a library GEMM, burst), for a dtype that file does not cover."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        g = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn(n, n, device="cuda", generator=g)
+        b = torch.randn(n, n, device="cuda", generator=g)
+        c = torch.empty(n, n, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(iters):
+            torch.matmul(a, b, out=c)
+        e1.record()
+        torch.cuda.synchronize()
+        sec = e0.elapsed_time(e1) * 1e-3 / iters
+        del a, b, c
+        return 2.0 * n ** 3 / sec / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
 
 
 def roofline_entry(nsm, plan, info, tf32, hbm_bound, ns_ms, ns_launches, algorithmic, executed, ns_bytes,
@@ -628,15 +657,19 @@ def run_gpu(args):
     algorithmic = sum(k * ns_flops(r, c)[1] for r, c, k in tensors)
     single_kernel = all(nsm.muon_get_bucket_info(plan, b).ns_single_kernel for b in range(info.n_buckets))
     executed = sum(k * ns_executed_flops(r, c, small=single_kernel) for r, c, k in tensors)
-    prep_bytes = sum(G[i].numel() * (G[i].element_size() + 4 + 4 + 2) for i in range(len(tensors)))
+    # G read, M read and written, X0 written: bf16, or in 3xTF32 mode fp32 hi and lo of X0 and X0^T
+    x0_bytes = 16 if tf32 else 2
+    prep_bytes = sum(G[i].numel() * (G[i].element_size() + 4 + 4 + x0_bytes) for i in range(len(tensors)))
     peaks, peak_kind = load_peaks()
     bf16_sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     peak_tf, peak_name = choose_bf16_peak(peaks, peak_kind, clocks, ms * 1e-3 * args.steps)
     ns_alg_tflops = algorithmic / (ns_ms * 1e-3) / 1e12
     if tf32:
-        # 3xTF32: three kind::tf32 products per product, against half the bf16 rate
-        peak_tf = tf32_peak(peak_tf)
-        peak_name = (f"{peak_name} x 0.5 (kind::tf32 measured at half the kind::f16 rate per SM); "
+        # 3xTF32: three kind::tf32 products per product, against cuBLAS's tf32 GEMM
+        # timed now (after the timed region, so it does not heat the GPU for it)
+        peak_tf = measure_tf32_gemm_tflops()
+        peak_name = ("cuBLAS tf32 GEMM measured in this run (torch.matmul, 8192^3 fp32 with TF32 "
+                     f"tensor cores, burst; half the bf16 figure would be {tf32_peak(peaks['bf16_tflops']):.1f}); "
                      "achieved counts the three tf32 products of each product")
     ns_launches = launches_per_step(nsm, plan, info, ns_only=True)
     # the single-launch kernel for m <= 128 reads X0 once and the weights once and

@@ -72,6 +72,29 @@ __device__ __forceinline__ void store_x(void* x_hi, float* x_lo, int64_t i, floa
   }
 }
 
+// Eight consecutive elements of X0 from index i (a multiple of 8 in a row of whole
+// 16-byte units): one 16-byte bf16 store, or two for each of the tf32 hi and lo parts.
+__device__ __forceinline__ void store_x8(void* x_hi, float* x_lo, int64_t i, const float v[8], int tf32) {
+  if (tf32) {
+    float h[8], l[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      h[j] = round_tf32(v[j]);
+      l[j] = v[j] - h[j];
+    }
+    float4* hp = reinterpret_cast<float4*>(reinterpret_cast<float*>(x_hi) + i);
+    float4* lp = reinterpret_cast<float4*>(x_lo + i);
+    hp[0] = make_float4(h[0], h[1], h[2], h[3]);
+    hp[1] = make_float4(h[4], h[5], h[6], h[7]);
+    lp[0] = make_float4(l[0], l[1], l[2], l[3]);
+    lp[1] = make_float4(l[4], l[5], l[6], l[7]);
+  } else {
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(x_hi) + i) =
+        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                   pack_bf16x2(v[6], v[7]));
+  }
+}
+
 // Thread (tx, ty) of a 64 x 64 tile: rows ty and ty + 32, columns 8 tx .. 8 tx + 7,
 // so that a full tile of a matrix whose rows are whole 16-byte units moves with
 // 16-byte accesses (bf16 G and X0: one per row; fp32 M: two per row).
@@ -175,10 +198,8 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
     for (int k = 0; k < 2; ++k) {
       const int64_t r = tile.r0 + ty + 32 * k;
       const int64_t c = tile.c0 + 8 * tx;
-      if (full && !a.tf32 && (ld & 7) == 0) {
-        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(hi) + base + r * ld + c) =
-            make_uint4(pack_bf16x2(v[k][0], v[k][1]), pack_bf16x2(v[k][2], v[k][3]),
-                       pack_bf16x2(v[k][4], v[k][5]), pack_bf16x2(v[k][6], v[k][7]));
+      if (full && (ld & 7) == 0) {
+        store_x8(hi, lo, base + r * ld + c, v[k], a.tf32);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -196,10 +217,8 @@ __global__ void __launch_bounds__(kThreads) momentum_prep_kernel(const __grid_co
       float w8[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) w8[j] = vt[8 * tx + j][xi];
-      if (full && !a.tf32 && (ld & 7) == 0) {
-        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(hi) + base + xr * ld + xc) =
-            make_uint4(pack_bf16x2(w8[0], w8[1]), pack_bf16x2(w8[2], w8[3]),
-                       pack_bf16x2(w8[4], w8[5]), pack_bf16x2(w8[6], w8[7]));
+      if (full && (ld & 7) == 0) {
+        store_x8(hi, lo, base + xr * ld + xc, w8, a.tf32);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
