@@ -34,6 +34,7 @@ WORKLOAD = ("qwen3-4b-layer: q 4096x2560, k/v 1024x2560, o 2560x4096, gate/up 97
             "down 2560x9728; G bf16 N(0,1e-3), M and W fp32 N(0,0.02); mu 0.95 Nesterov, lr 0.02, "
             "wd 0, 5 NS iterations (3.4445, -4.7750, 2.0315)")
 LR, MU, WD, NS_STEPS = 0.02, 0.95, 0.0, 5
+NS_COEFFS = (3.4445, -4.7750, 2.0315)
 # Newton-Schulz coefficients: "fixed" (the configuration's (a, b, c) every
 # iteration) or "minimax" (per-iteration schedule, see --ns-schedule); set by main()
 NS_SCHEDULE = {"kind": "fixed", "lower": 1e-3, "safety": 1.05}
@@ -569,6 +570,46 @@ def workload_spec(name, layers=None):
     raise ValueError(name)
 
 
+def library_step(torch, W, M, G, coeffs, lr=LR, mu=MU, wd=WD, eps=1e-7):
+    """The same Muon step written the way the pages run it, with library kernels: a
+    Python loop over the workload's tensors, each a batch of same-shape logical
+    matrices, doing fp32 EMA momentum with Nesterov look-ahead, the Frobenius norm, the
+    bf16 cast and the quintic iterations as batched bf16 GEMMs (cuBLAS on the GPU, fp32
+    accumulation; b A + c A A and a X + B X through the GEMMs' beta), then the scaled
+    weight update.  A timing reference for the hand-written kernels, not a product
+    path."""
+    for w, m, g in zip(W, M, G):
+        m.mul_(mu).add_(g, alpha=1.0 - mu)
+        v = m * mu
+        v.add_(g, alpha=1.0 - mu)
+        tall = v.shape[-2] > v.shape[-1]
+        x = v.mT if tall else v
+        nrm = torch.linalg.vector_norm(x, dim=(-2, -1), keepdim=True).add_(eps)
+        x = (x / nrm).to(torch.bfloat16)
+        for a, b, c in coeffs:
+            A = torch.bmm(x, x.mT)
+            B = torch.baddbmm(A, A, A, beta=b, alpha=c)
+            x = torch.baddbmm(x, B, x, beta=a)
+        u = x.mT if tall else x
+        scale = math.sqrt(max(1.0, w.shape[-2] / w.shape[-1]))
+        if wd:
+            w.mul_(1.0 - lr * wd)
+        w.add_(u.to(w.dtype), alpha=-lr * scale)
+
+
+def library_step_ms(torch, W, M, G, steps, coeffs):
+    """CUDA-event time of library_step (one untimed step first); W and M are left changed."""
+    library_step(torch, W, M, G, coeffs)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        library_step(torch, W, M, G, coeffs)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -781,6 +822,14 @@ def run_gpu(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if not args.no_library_baseline and not tf32 and NS_METHOD == "standard" and NS_SCHEDULE["kind"] == "fixed":
+        k_lib = max(1, min(args.steps, 10 if args.workload != "experts" else 2))
+        lib_ms = max_over_ranks([library_step_ms(torch, W, M, G, k_lib, [NS_COEFFS] * NS_STEPS)])[0]
+        line["library_baseline"] = {
+            "value": whole_job_rate(n_mats, world, lib_ms), "unit": "matrices/s", "ms_per_step": lib_ms,
+            "steps": k_lib, "speedup_of_value": lib_ms / ms,
+            "what": "the same step as a per-tensor loop of torch ops on this GPU (cuBLAS bf16 batched GEMMs "
+                    "with fp32 accumulation, fp32 momentum and norm), timed after the measurements above"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_leg(args.workload)
     if rank == 0:
@@ -900,6 +949,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-library-baseline", action="store_true",
+                    help="skip timing the same step as a loop of torch (cuBLAS) ops on the GPU")
     ap.add_argument("--workload", choices=["layer", "single", "heads", "experts", "offload"], default="layer",
                     help="layer (default, the headline) or another measured workload")
     ap.add_argument("--ns-precision", choices=["bf16", "tf32x3"], default="bf16",
