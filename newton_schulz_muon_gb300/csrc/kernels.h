@@ -189,6 +189,10 @@ struct SmallArgs {
   int32_t n_psegs;
   int32_t* flags;        // per bucket-local matrix: 1 if the norm was not finite (fuse_prep)
   SmallPrepSeg pseg[kMaxSegs];
+  // start stagger (performance only): CTAs with blockIdx.x >= stagger_from wait
+  // stagger_ns after their set-up before taking their first matrix
+  int32_t stagger_from;
+  int64_t stagger_ns;
 };
 
 // GEMM tile shape (bf16): 128 x 256 outputs per CTA, 64-deep k blocks.

@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) ns_gram_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  start_stagger(a);
   const uint32_t tmem = tmem_slot;
   uint8_t* ring = smem + kOffRingG;
 

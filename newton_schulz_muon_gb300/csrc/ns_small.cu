@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) ns_small_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  start_stagger(a);
   const uint32_t tmem = tmem_slot;
   uint8_t* ring = smem + kOffRing;
 

@@ -34,6 +34,24 @@ constexpr uint32_t kPrepSlot = kPrepG + 128u * 128u;   // 24 KB
 constexpr int kPrepSlots = 4;
 static_assert(kChunkCols == 4 * kPrepCols, "four quarters per chunk");
 
+// Start stagger.  Every CTA of these kernels takes its matrices in the same order
+// of phases: X0 streamed in from HBM, iterations that mostly hit the L2, and a
+// last pass that streams the weights from and back to HBM.  CTAs that start
+// together stay in step, so their HBM-heavy passes coincide and leave HBM idle in
+// between.  The CTAs with one matrix fewer than the others (blockIdx.x >=
+// stagger_from) start stagger_ns later, which they can spare, so that their
+// matrix boundaries fall inside the others' iterations (when every CTA has as
+// many matrices, the second half of them waits).  Performance only: no result
+// depends on it.  The condition is the same for every thread of a CTA.
+__device__ __forceinline__ void start_stagger(const SmallArgs& a) {
+  if (a.stagger_ns <= 0 || (int)blockIdx.x < a.stagger_from) return;
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < (unsigned long long)a.stagger_ns) __nanosleep(1000);
+  }
+  __syncthreads();
+}
+
 // Byte offset of 16-byte piece `piece` (8 bf16) of row r in a 128-byte-swizzled
 // tile of 128-byte rows (1024-byte aligned).
 __device__ __forceinline__ uint32_t sw128(int r, int piece) {
