@@ -366,10 +366,10 @@ class ClockSampler:
 GEMM_SOURCES = ['newton_schulz_muon_gb300/csrc/ns_gemm.cu', 'newton_schulz_muon_gb300/csrc/device.cuh', 'newton_schulz_muon_gb300/csrc/kernels.h', 'newton_schulz_muon_gb300/csrc/epilogue.cuh']
 GRAM_SOURCES = ['newton_schulz_muon_gb300/csrc/ns_gram.cu', 'newton_schulz_muon_gb300/csrc/small_common.cuh', 'newton_schulz_muon_gb300/csrc/device.cuh', 'newton_schulz_muon_gb300/csrc/kernels.h', 'newton_schulz_muon_gb300/csrc/epilogue.cuh', 'newton_schulz_muon_gb300/csrc/momentum.cuh']
 SMALL_SOURCES = ['newton_schulz_muon_gb300/csrc/ns_small.cu', 'newton_schulz_muon_gb300/csrc/small_common.cuh', 'newton_schulz_muon_gb300/csrc/device.cuh', 'newton_schulz_muon_gb300/csrc/kernels.h', 'newton_schulz_muon_gb300/csrc/epilogue.cuh', 'newton_schulz_muon_gb300/csrc/momentum.cuh']
-NS_GEMM_TRAFFIC = {"bytes_per_launch": 346.9e6, "sources_sha256_16": "9940b3a8090a4f28"}
+NS_GEMM_TRAFFIC = {"bytes_per_launch": 349.8e6, "sources_sha256_16": "fedaaee9110f4a6f"}
 HEAD_TRAFFIC = {
-    "gram": {"bytes_per_matrix": (854.2e6 + 386.6e6) / 336, "sources_sha256_16": "8454c4b5272221c8"},
-    "standard": {"bytes_per_matrix": (880.5e6 + 748.4e6) / 336, "sources_sha256_16": "011243bf1e9f7d91"},
+    "gram": {"bytes_per_matrix": (867.9e6 + 385.2e6) / 336, "sources_sha256_16": "85e08252a0e7d041"},
+    "standard": {"bytes_per_matrix": (987.3e6 + 840.0e6) / 336, "sources_sha256_16": "ae082159e25b58f0"},
 }
 
 
