@@ -211,7 +211,13 @@ muon_status muon_polar_express_coefficients(int32_t n_iters, double lower, doubl
  *   nesterov:         0 / 1.
  *   ns_steps:         Newton-Schulz iterations (0..16); the pages use 5-6.
  * Arguments are validated before anything is enqueued.  The buffers of one
- * entry must not overlap another entry's.  Returns MUON_OK after enqueueing. */
+ * entry must not overlap another entry's.  Returns MUON_OK after enqueueing.
+ * The call only launches kernels on `stream` (no host synchronisation, no
+ * allocation), so one step can be captured with stream capture into a CUDA
+ * graph and replayed: every replay uses the captured pointers, lr, mu, wd and
+ * ns_steps, and reads whatever the captured gradient buffers then hold (tested
+ * with cfg.timing = 0; one plan's steps, captured or not, must not overlap on
+ * the device, since they share its workspace). */
 muon_status muon_step(muon_plan_t* plan, void* const* params, const void* const* grads,
                       void* const* momentum, int64_t n_mats, float lr, float mu,
                       int32_t nesterov, float wd, int32_t ns_steps, void* stream);
