@@ -651,13 +651,17 @@ muon_status enqueue_ns_small(muon_plan_t* p, const Bucket& b, int ns_steps, cuda
     // the gram kernel (1728 per-head matrices of 20 chunks: fastest between 45 and
     // 60 us; two or three stagger groups were no faster than one).  The CTAs with
     // one matrix fewer wait; when every CTA has as many matrices, the second half
-    // waits (1824 matrices, 12 per CTA: 4% faster all the same); a single wave of
-    // matrices is not staggered.
+    // waits (1824 matrices, 12 per CTA: 4% faster all the same), but only from four
+    // matrices per CTA on, where the wait is a small part of a CTA's time; a single
+    // wave of matrices is not staggered.
     const int32_t grid = units < p->num_sms ? units : p->num_sms;
     int64_t max_n = 0;
     for (const BGroup& g : b.groups) max_n = std::max<int64_t>(max_n, g.n);
     const int64_t chunks = (max_n + 127) / 128;
-    sa.stagger_from = units <= grid ? INT32_MAX : units % grid ? units % grid : grid / 2;
+    sa.stagger_from = units <= grid                     ? INT32_MAX
+                      : units % grid                    ? units % grid
+                      : units >= 4 * (int64_t)grid      ? grid / 2
+                                                        : INT32_MAX;
     sa.stagger_ns = std::min<int64_t>(200000, 3000 * chunks);
   }
   sa.ns_steps = ns_steps;
