@@ -368,8 +368,8 @@ GRAM_SOURCES = ['newton_schulz_muon_gb300/csrc/ns_gram.cu', 'newton_schulz_muon_
 SMALL_SOURCES = ['newton_schulz_muon_gb300/csrc/ns_small.cu', 'newton_schulz_muon_gb300/csrc/small_common.cuh', 'newton_schulz_muon_gb300/csrc/device.cuh', 'newton_schulz_muon_gb300/csrc/kernels.h', 'newton_schulz_muon_gb300/csrc/epilogue.cuh', 'newton_schulz_muon_gb300/csrc/momentum.cuh']
 NS_GEMM_TRAFFIC = {"bytes_per_launch": 349.8e6, "sources_sha256_16": "fedaaee9110f4a6f"}
 HEAD_TRAFFIC = {
-    "gram": {"bytes_per_matrix": (867.9e6 + 385.2e6) / 336, "sources_sha256_16": "85e08252a0e7d041"},
-    "standard": {"bytes_per_matrix": (987.3e6 + 840.0e6) / 336, "sources_sha256_16": "ae082159e25b58f0"},
+    "gram": {"bytes_per_matrix": (868.6e6 + 385.4e6) / 336, "sources_sha256_16": "0f481e2ae9140ef6"},
+    "standard": {"bytes_per_matrix": (993.6e6 + 846.1e6) / 336, "sources_sha256_16": "1a27241ab7278f8c"},
 }
 
 

@@ -46,8 +46,9 @@ static_assert(kChunkCols == 4 * kPrepCols, "four quarters per chunk");
 __device__ __forceinline__ void start_stagger(const SmallArgs& a) {
   if (a.stagger_ns <= 0 || (int)blockIdx.x < a.stagger_from) return;
   if (threadIdx.x == 0) {
+    // bounded by a count as well as by the clock (a few thousand 1 us sleeps at most)
     const unsigned long long t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < (unsigned long long)a.stagger_ns) __nanosleep(1000);
+    for (int i = 0; i < 4096 && globaltimer_ns() - t0 < (unsigned long long)a.stagger_ns; ++i) __nanosleep(1000);
   }
   __syncthreads();
 }
