@@ -163,6 +163,19 @@ def test_more_matrices_than_ctas(m, kernel):
     run_steps(m, wl, cfg=_cfg(m, k), cap=0)
 
 
+@pytest.mark.parametrize("waves, extra", [(4, 0), (2, 5)])
+def test_start_stagger_cases(m, waves, extra):
+    # matrix counts that take each branch of the start stagger: every CTA with as many
+    # matrices, from four per CTA (the second half of the CTAs start later), and some
+    # CTAs with one matrix fewer (those start later); no result depends on it
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = Workload([(128, 256, waves * sms + extra)], m_sigma=0.02, g_sigma=1e-3)
+    run_steps(m, wl, cfg=_cfg(m, m.MUON_NS_KERNEL_AUTO), cap=0)
+    wl = Workload([(96, 512, waves * sms + extra)], m_sigma=0.02, g_sigma=1e-3)
+    run_steps(m, wl, cfg=m.muon_config_default(ns_method=m.MUON_NS_METHOD_GRAM), cap=0, method="gram")
+
+
 @pytest.mark.parametrize("ns_steps", [1, 2, 6])
 def test_iteration_counts(m, ns_steps):
     wl = Workload([(128, 1024, 2), (64, 333)], m_sigma=0.02, g_sigma=1e-3)
